@@ -1,0 +1,491 @@
+// mla_api.cu -- the C ABI of libmla_gb300.so: host-side validation, the row
+// plan / shard row view integer kernels, the device error word, TMA
+// descriptor encoding and the decode -> segment-merge sequence.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "mla_gb300.h"
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+thread_local char g_last_error[512] = "";
+__device__ int g_device_error;  // first device-detected problem (mla_device_error)
+int *g_err_ptr[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+__device__ __forceinline__ void dev_error(int *err, int code) { atomicCAS(err, 0, code); }
+
+// Round-robin count of window w on rank r of W (interleave 1): positions
+// g < w with g mod W == r, i.e. floor((w - 1 - r) / W) + 1 when w - 1 - r >= 0.
+// [vLLM #51705 digest, _build_dcp_verify_row_view snippet; sglang #34432,
+// g(j) = j * W + r]
+__device__ __forceinline__ int rr_count(int w, int W, int r) {
+  const int top = w - 1 - r;
+  return top >= 0 ? top / W + 1 : 0;
+}
+
+// Request owning row r: the b with qo_indptr[b] <= r < qo_indptr[b+1].
+__device__ __forceinline__ int find_request(const int32_t *ind, int B, int r) {
+  int lo = 0, hi = B;  // invariant: ind[lo] <= r < ind[hi] when indptr is valid
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (ind[mid] <= r) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Row plan: row t of request b sees global positions [0, L_b - qlen_b + t]
+// [vLLM #51705 digest, 实现拆解 2].
+__global__ void plan_rows_kernel(int B, int T, const int32_t *seq_lens, const int32_t *ind,
+                                 int32_t *row_len, int32_t *row_req, int *err) {
+  const int total = ind[B];
+  const bool ind_ok = ind[0] == 0 && total >= 0 && total <= T;
+  const int stride = gridDim.x * blockDim.x;
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += stride) {
+    const int qlen = ind[b + 1] - ind[b];
+    if (qlen < 0) dev_error(err, MLA_DEV_BAD_INDPTR);
+    else if (qlen == 0 || qlen > seq_lens[b]) dev_error(err, MLA_DEV_BAD_QLEN);
+  }
+  if (!ind_ok) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) dev_error(err, MLA_DEV_BAD_INDPTR);
+  }
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < T; r += stride) {
+    if (!ind_ok || r >= total) {
+      row_len[r] = 0;
+      row_req[r] = -1;
+      continue;
+    }
+    const int b = find_request(ind, B, r);
+    const int qlen = ind[b + 1] - ind[b];
+    const int L = seq_lens[b];
+    const int t = r - ind[b];
+    const bool good = qlen >= 1 && qlen <= L && t >= 0 && t < qlen;
+    row_len[r] = good ? L - qlen + 1 + t : 0;
+    row_req[r] = b;
+  }
+}
+
+// Shard row view: per-row shard-local count from the row's global window.
+__global__ void shard_rows_kernel(int B, int T, const int32_t *ind, const int32_t *row_len_global,
+                                  int W, int rank, int32_t *row_len_local, int *err) {
+  const int total = ind[B];
+  const bool ind_ok = ind[0] == 0 && total >= 0 && total <= T;
+  if (!ind_ok && blockIdx.x == 0 && threadIdx.x == 0) dev_error(err, MLA_DEV_BAD_INDPTR);
+  const int stride = gridDim.x * blockDim.x;
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < T; r += stride) {
+    row_len_local[r] = (ind_ok && r < total) ? rr_count(row_len_global[r], W, rank) : 0;
+  }
+}
+
+// Sub-page table [vLLM #51705 digest, 实现拆解 3]: local page p of request b is
+// block_table[b][p / R] * R + p % R (R = block_size / P) for the pages that
+// hold the request's longest row, -1 after that.
+__global__ void subpage_table_kernel(int B, const int32_t *ind, const int32_t *row_len,
+                                     const int32_t *bt, int bt_stride, int num_blocks,
+                                     int block_size, int P, int32_t *sp, int sp_stride, int *err) {
+  const int b = blockIdx.x;
+  if (b >= B) return;
+  __shared__ int s_pages;
+  if (threadIdx.x == 0) {
+    int len = 0;
+    const int r0 = ind[b], r1 = ind[b + 1];
+    if (r0 >= 0 && r1 >= r0)
+      for (int r = r0; r < r1; ++r) len = max(len, row_len[r]);
+    int pages = (len + P - 1) / P;
+    if (pages > sp_stride) {
+      dev_error(err, MLA_DEV_LEN_BOUND);
+      pages = sp_stride;
+    }
+    s_pages = pages;
+  }
+  __syncthreads();
+  const int pages = s_pages;
+  const int R = block_size / P;
+  int32_t *row = sp + static_cast<int64_t>(b) * sp_stride;
+  for (int pg = threadIdx.x; pg < sp_stride; pg += blockDim.x) {
+    int32_t v = -1;
+    if (pg < pages) {
+      const int bi = pg / R;
+      const int blk = bi < bt_stride ? bt[static_cast<int64_t>(b) * bt_stride + bi] : -1;
+      if (blk < 0 || blk >= num_blocks) dev_error(err, MLA_DEV_BAD_BLOCK_ID);
+      else v = blk * R + pg % R;
+    }
+    row[pg] = v;
+  }
+}
+
+int grid_for(int n, int threads) {
+  int g = (n + threads - 1) / threads;
+  return g < 1 ? 1 : (g > 1024 ? 1024 : g);
+}
+
+bool is_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+void set_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+}
+
+mla_status cuda_fail(cudaError_t e, const char *what) {
+  set_error("%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  return MLA_ERR_CUDA;
+}
+
+int *device_error_word() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "cudaGetDevice");
+    return nullptr;
+  }
+  if (dev < 0 || dev >= 64) {
+    set_error("device ordinal %d out of range", dev);
+    return nullptr;
+  }
+  if (g_err_ptr[dev] == nullptr) {
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_device_error);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+      return nullptr;
+    }
+    g_err_ptr[dev] = static_cast<int *>(ptr);
+  }
+  return g_err_ptr[dev];
+}
+
+mla_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                        int elem_bytes, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                        uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  if (g_encode == nullptr) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      set_error("cuTensorMapEncodeTiled entry point unavailable");
+      return MLA_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * static_cast<uint64_t>(elem_bytes)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (CUresult %d): rows=%llu cols=%llu box=%ux%u", (int)r,
+              (unsigned long long)rows, (unsigned long long)cols, box_cols, box_rows);
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+mla_status launch_plan_rows(int B, int T, const int32_t *seq_lens, const int32_t *ind,
+                            int32_t *row_len, int32_t *row_req, int *err, cudaStream_t stream) {
+  const int n = T > B ? T : B;
+  plan_rows_kernel<<<grid_for(n, 256), 256, 0, stream>>>(B, T, seq_lens, ind, row_len, row_req, err);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan_rows launch");
+}
+
+mla_status launch_shard_rows(int B, int T, const int32_t *ind, const int32_t *row_len_global,
+                             int W, int rank, int32_t *row_len_local, int *err,
+                             cudaStream_t stream) {
+  shard_rows_kernel<<<grid_for(T, 256), 256, 0, stream>>>(B, T, ind, row_len_global, W, rank,
+                                                           row_len_local, err);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "shard_row_view launch");
+}
+
+mla_status launch_subpage_table(int B, const int32_t *ind, const int32_t *row_len,
+                                const int32_t *bt, int bt_stride, int num_blocks, int block_size,
+                                int P, int32_t *sp, int sp_stride, int *err, cudaStream_t stream) {
+  if (B == 0) return MLA_OK;
+  subpage_table_kernel<<<B, 128, 0, stream>>>(B, ind, row_len, bt, bt_stride, num_blocks,
+                                              block_size, P, sp, sp_stride, err);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "subpage_table launch");
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+const char *mla_last_error_string(void) { return g_last_error; }
+
+const char *mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_DEVICE_CHECK: return "MLA_ERR_DEVICE_CHECK";
+    default: return "MLA_STATUS_UNKNOWN";
+  }
+}
+
+int mla_page_size(int block_size) {
+  if (block_size <= 0) return -1;
+  const int low_bit = block_size & -block_size;  // largest power-of-two divisor
+  return low_bit < 128 ? low_bit : 128;
+}
+
+static mla_status check_table_args(const int32_t *block_table, int bt_stride, int num_blocks,
+                                   int block_size, const int32_t *sp, int sp_stride, int *P_out) {
+  const int P = mla_page_size(block_size);
+  if (P < 0) {
+    set_error("block_size must be positive (got %d)", block_size);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (block_table != nullptr) {
+    if (bt_stride < 1 || num_blocks < 1 || sp == nullptr || sp_stride < 1) {
+      set_error("block table given but block_table_stride=%d num_blocks=%d subpage_stride=%d",
+                bt_stride, num_blocks, sp_stride);
+      return MLA_ERR_INVALID_ARG;
+    }
+    if (static_cast<int64_t>(num_blocks) * (block_size / P) > INT32_MAX) {
+      set_error("num_blocks * (block_size / page_size) overflows int32 sub-page ids");
+      return MLA_ERR_INVALID_ARG;
+    }
+  }
+  *P_out = P;
+  return MLA_OK;
+}
+
+mla_status mla_plan_rows(int num_reqs, int num_rows, const int32_t *seq_lens,
+                         const int32_t *qo_indptr, int32_t *row_len, int32_t *row_req,
+                         const int32_t *block_table, int block_table_stride, int num_blocks,
+                         int block_size, int32_t *subpage_table, int subpage_stride,
+                         mla_stream_t stream) {
+  if (num_reqs < 0 || num_rows < 0 || qo_indptr == nullptr ||
+      (num_reqs > 0 && seq_lens == nullptr) || (num_rows > 0 && (row_len == nullptr || row_req == nullptr))) {
+    set_error("mla_plan_rows: bad sizes or null pointers (B=%d T=%d)", num_reqs, num_rows);
+    return MLA_ERR_INVALID_ARG;
+  }
+  int P = 0;
+  if (block_table != nullptr) {
+    mla_status st = check_table_args(block_table, block_table_stride, num_blocks, block_size,
+                                     subpage_table, subpage_stride, &P);
+    if (st != MLA_OK) return st;
+  }
+  int *err = device_error_word();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mla_status st = launch_plan_rows(num_reqs, num_rows, seq_lens, qo_indptr, row_len, row_req, err, s);
+  if (st != MLA_OK || block_table == nullptr) return st;
+  return launch_subpage_table(num_reqs, qo_indptr, row_len, block_table, block_table_stride,
+                              num_blocks, block_size, P, subpage_table, subpage_stride, err, s);
+}
+
+mla_status mla_shard_row_view(int num_reqs, int num_rows, const int32_t *qo_indptr,
+                              const int32_t *row_len_global, int world_size, int rank,
+                              int interleave, int32_t *row_len_local, const int32_t *block_table,
+                              int block_table_stride, int num_blocks, int block_size,
+                              int32_t *subpage_table, int subpage_stride, mla_stream_t stream) {
+  if (interleave != 1) {
+    set_error("mla_shard_row_view: only round-robin interleave 1 is supported (got %d)", interleave);
+    return MLA_ERR_UNSUPPORTED;
+  }
+  if (world_size < 1 || rank < 0 || rank >= world_size) {
+    set_error("mla_shard_row_view: rank %d of world_size %d", rank, world_size);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (num_reqs < 0 || num_rows < 0 || qo_indptr == nullptr ||
+      (num_rows > 0 && (row_len_global == nullptr || row_len_local == nullptr))) {
+    set_error("mla_shard_row_view: bad sizes or null pointers (B=%d T=%d)", num_reqs, num_rows);
+    return MLA_ERR_INVALID_ARG;
+  }
+  int P = 0;
+  if (block_table != nullptr) {
+    mla_status st = check_table_args(block_table, block_table_stride, num_blocks, block_size,
+                                     subpage_table, subpage_stride, &P);
+    if (st != MLA_OK) return st;
+  }
+  int *err = device_error_word();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mla_status st = launch_shard_rows(num_reqs, num_rows, qo_indptr, row_len_global, world_size,
+                                    rank, row_len_local, err, s);
+  if (st != MLA_OK || block_table == nullptr) return st;
+  return launch_subpage_table(num_reqs, qo_indptr, row_len_local, block_table, block_table_stride,
+                              num_blocks, block_size, P, subpage_table, subpage_stride, err, s);
+}
+
+static mla_status check_decode_args(const mla_decode_args *a) {
+  if (a == nullptr) {
+    set_error("mla_decode_verify: null argument struct");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (a->num_reqs < 1 || a->num_rows < 1 || a->num_heads < 1 || a->max_qlen < 1 ||
+      a->num_segments < 1 || a->subpage_stride < 1 || a->num_cache_rows < 1) {
+    set_error("mla_decode_verify: B=%d T=%d H=%d max_qlen=%d S=%d subpage_stride=%d rows=%lld must be >= 1",
+              a->num_reqs, a->num_rows, a->num_heads, a->max_qlen, a->num_segments,
+              a->subpage_stride, (long long)a->num_cache_rows);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (a->kv_dtype != MLA_KV_BF16 && a->kv_dtype != MLA_KV_FP8_E4M3) {
+    set_error("mla_decode_verify: unknown kv_dtype %d", a->kv_dtype);
+    return MLA_ERR_UNSUPPORTED;
+  }
+  if (a->page_size < 8 || a->page_size > 128 || (a->page_size & (a->page_size - 1)) != 0) {
+    set_error("mla_decode_verify: page_size %d unsupported (power of two in [8, 128])", a->page_size);
+    return MLA_ERR_UNSUPPORTED;
+  }
+  if (static_cast<int64_t>(a->subpage_stride) * a->page_size > INT32_MAX ||
+      a->num_cache_rows > INT32_MAX || static_cast<int64_t>(a->num_rows) * a->num_heads > INT32_MAX) {
+    set_error("mla_decode_verify: sizes overflow int32 indexing");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (a->num_segments > 65535 || a->num_reqs > 65535 ||
+      (static_cast<int64_t>(a->max_qlen) * a->num_heads + 63) / 64 > 65535) {
+    set_error("mla_decode_verify: grid too large (S=%d B=%d max_qlen*H=%lld)", a->num_segments,
+              a->num_reqs, (long long)a->max_qlen * a->num_heads);
+    return MLA_ERR_UNSUPPORTED;
+  }
+  if (a->q == nullptr || a->kv_cache == nullptr || a->qo_indptr == nullptr || a->row_len == nullptr ||
+      a->subpage_table == nullptr || a->out == nullptr || a->lse == nullptr) {
+    set_error("mla_decode_verify: null device pointer");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!is_aligned(a->q, 16) || !is_aligned(a->kv_cache, 16) || !is_aligned(a->out, 16)) {
+    set_error("mla_decode_verify: q, kv_cache and out must be 16-byte aligned");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if ((a->flags & ~MLA_DECODE_SKIP_MERGE) != 0) {
+    set_error("mla_decode_verify: unknown flags 0x%x", a->flags);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!(a->sm_scale > 0.0f) || (a->kv_dtype == MLA_KV_FP8_E4M3 && !(a->kv_scale > 0.0f))) {
+    set_error("mla_decode_verify: sm_scale and (fp8) kv_scale must be positive");
+    return MLA_ERR_INVALID_ARG;
+  }
+  return MLA_OK;
+}
+
+size_t mla_decode_verify_workspace(const mla_decode_args *a) {
+  if (a == nullptr || a->num_segments <= 1 || a->num_rows < 1 || a->num_heads < 1) return 0;
+  const size_t items = static_cast<size_t>(a->num_rows) * a->num_heads * a->num_segments;
+  return align256(items * 512 * sizeof(float)) + 2 * align256(items * sizeof(float));
+}
+
+mla_status mla_decode_verify(const mla_decode_args *a, void *workspace, size_t workspace_bytes,
+                             mla_stream_t stream) {
+  mla_status st = check_decode_args(a);
+  if (st != MLA_OK) return st;
+  const size_t need = mla_decode_verify_workspace(a);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !is_aligned(workspace, 256))) {
+    set_error("mla_decode_verify: workspace of %zu bytes (256-byte aligned) needed, got %zu at %p",
+              need, workspace_bytes, workspace);
+    return MLA_ERR_WORKSPACE;
+  }
+  int *err = device_error_word();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DecodeLaunch d{};
+  d.a = a;
+  d.err = err;
+  if (need > 0) {
+    const size_t items = static_cast<size_t>(a->num_rows) * a->num_heads * a->num_segments;
+    char *w = static_cast<char *>(workspace);
+    d.segm_out = reinterpret_cast<float *>(w);
+    d.segm_max = reinterpret_cast<float *>(w + align256(items * 512 * sizeof(float)));
+    d.segm_sum = reinterpret_cast<float *>(w + align256(items * 512 * sizeof(float)) +
+                                           align256(items * sizeof(float)));
+  }
+  st = launch_decode(d, s);
+  if (st != MLA_OK || need == 0 || (a->flags & MLA_DECODE_SKIP_MERGE)) return st;
+  MergeLaunch m{};
+  m.mode = MLA_MERGE_SEGMENTS;
+  m.num_rows = a->num_rows;
+  m.num_heads = a->num_heads;
+  m.num_parts = a->num_segments;
+  m.segm_out = d.segm_out;
+  m.segm_max = d.segm_max;
+  m.segm_sum = d.segm_sum;
+  m.out = a->out;
+  m.lse = a->lse;
+  m.live_rows = a->qo_indptr + a->num_reqs;
+  return launch_merge(m, s);
+}
+
+mla_status mla_merge_segments(const mla_merge_args *a, mla_stream_t stream) {
+  if (a == nullptr || a->num_rows < 0 || a->num_heads < 1 || a->num_parts < 1 ||
+      a->out == nullptr || a->lse == nullptr) {
+    set_error("mla_merge_segments: bad arguments");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (a->mode == MLA_MERGE_SEGMENTS) {
+    if (a->segm_out == nullptr || a->segm_max == nullptr || a->segm_sum == nullptr ||
+        !is_aligned(a->segm_out, 16)) {
+      set_error("mla_merge_segments: segment mode needs 16-byte aligned segm_out, segm_max, segm_sum");
+      return MLA_ERR_INVALID_ARG;
+    }
+  } else if (a->mode == MLA_MERGE_STATES) {
+    if (a->part_out == nullptr || a->part_lse == nullptr || !is_aligned(a->part_out, 16)) {
+      set_error("mla_merge_segments: state mode needs 16-byte aligned part_out and part_lse");
+      return MLA_ERR_INVALID_ARG;
+    }
+  } else {
+    set_error("mla_merge_segments: unknown mode %d", a->mode);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!is_aligned(a->out, 16)) {
+    set_error("mla_merge_segments: out must be 16-byte aligned");
+    return MLA_ERR_INVALID_ARG;
+  }
+  MergeLaunch m{};
+  m.mode = a->mode;
+  m.num_rows = a->num_rows;
+  m.num_heads = a->num_heads;
+  m.num_parts = a->num_parts;
+  m.segm_out = a->segm_out;
+  m.segm_max = a->segm_max;
+  m.segm_sum = a->segm_sum;
+  m.part_out = a->part_out;
+  m.part_lse = a->part_lse;
+  m.out = a->out;
+  m.lse = a->lse;
+  m.live_rows = nullptr;
+  return launch_merge(m, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_get_device_error(int32_t *code_out, mla_stream_t stream) {
+  if (code_out == nullptr) {
+    set_error("mla_get_device_error: null code_out");
+    return MLA_ERR_INVALID_ARG;
+  }
+  *code_out = 0;
+  int *err = device_error_word();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int code = 0;
+  cudaError_t e = cudaMemcpyAsync(&code, err, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "mla_get_device_error");
+  *code_out = code;
+  return code == 0 ? MLA_OK : MLA_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// mla_internal.h -- declarations shared by the translation units of
+// libmla_gb300.so (host launchers, error plumbing).  Not part of the C ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mla_gb300.h"
+
+namespace mla {
+
+// Records a printf-style message as the calling thread's last error text.
+void set_error(const char *fmt, ...);
+// Records a CUDA runtime failure and returns MLA_ERR_CUDA.
+mla_status cuda_fail(cudaError_t e, const char *what);
+
+// Device address of the library's device error word on the current device
+// (looked up once per device); nullptr after recording an error.
+int *device_error_word();
+
+// Encodes a 2-D tiled TMA descriptor over a row-major [rows, cols] matrix.
+mla_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                        int elem_bytes, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                        uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
+// Launchers (arguments already validated on the host).
+mla_status launch_plan_rows(int num_reqs, int num_rows, const int32_t *seq_lens,
+                            const int32_t *qo_indptr, int32_t *row_len, int32_t *row_req,
+                            int *err, cudaStream_t stream);
+mla_status launch_shard_rows(int num_reqs, int num_rows, const int32_t *qo_indptr,
+                             const int32_t *row_len_global, int world_size, int rank,
+                             int32_t *row_len_local, int *err, cudaStream_t stream);
+mla_status launch_subpage_table(int num_reqs, const int32_t *qo_indptr, const int32_t *row_len,
+                                const int32_t *block_table, int bt_stride, int num_blocks,
+                                int block_size, int page_size, int32_t *subpage_table,
+                                int sp_stride, int *err, cudaStream_t stream);
+
+struct DecodeLaunch {
+  const mla_decode_args *a;
+  float *segm_out;
+  float *segm_max;
+  float *segm_sum;
+  int *err;
+};
+mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream);
+
+struct MergeLaunch {
+  int mode;
+  int num_rows;
+  int num_heads;
+  int num_parts;
+  const float *segm_out;
+  const float *segm_max;
+  const float *segm_sum;
+  const void *part_out;
+  const float *part_lse;
+  void *out;
+  float *lse;
+  const int32_t *live_rows;  // optional device int: rows (t) actually present; nullptr = all
+};
+mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream);
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace mla

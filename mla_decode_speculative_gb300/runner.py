@@ -1,0 +1,99 @@
+"""The whole decode / verify step through the C ABI, with buffers allocated once.
+
+``VerifyStep`` owns every device buffer one step needs (row plan, sub-page
+tables, split-K workspace, shard partial states, outputs), sized by static
+bounds, so a step issues only library launches and can be captured in a CUDA
+graph.  Unsharded step: mla_plan_rows (+ sub-page expansion) ->
+mla_decode_verify (decode + segment merge).  Context-sharded step (W round-robin
+shards simulated on one device): mla_plan_rows (global windows) -> per shard
+mla_shard_row_view + mla_decode_verify into a [W, T, H, .] state buffer ->
+mla_merge_segments (state mode).
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import mla
+
+
+class VerifyStep:
+    def __init__(self, *, num_reqs: int, num_rows: int, num_heads: int, max_qlen: int,
+                 block_size: int, num_blocks: int, block_table_width: int, max_kv_len: int,
+                 num_segments: int = 1, world_size: int = 1, kv_fp8: bool = False,
+                 device="cuda"):
+        self.B, self.T, self.H = num_reqs, num_rows, num_heads
+        self.max_qlen = max_qlen
+        self.block_size = block_size
+        self.num_blocks = num_blocks
+        self.W = world_size
+        self.S = num_segments
+        self.P = mla.page_size(block_size)
+        self.sp_stride = max(1, -(-max_kv_len // self.P))
+        self.kv_fp8 = kv_fp8
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.row_len = torch.empty(num_rows, **i32)
+        self.row_req = torch.empty(num_rows, **i32)
+        self.subpage = torch.empty((world_size, num_reqs, self.sp_stride), **i32)
+        self.row_len_local = torch.empty((world_size, num_rows), **i32)
+        self.out = torch.empty((num_rows, num_heads, mla.D_V), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((num_rows, num_heads), dtype=torch.float32, device=dev)
+        if world_size > 1:
+            self.part_out = torch.empty((world_size, num_rows, num_heads, mla.D_V),
+                                        dtype=torch.bfloat16, device=dev)
+            self.part_lse = torch.empty((world_size, num_rows, num_heads), dtype=torch.float32,
+                                        device=dev)
+        ws = 0
+        if num_segments > 1:
+            items = num_rows * num_heads * num_segments
+            ws = ((items * 512 * 4 + 255) & ~255) + 2 * ((items * 4 + 255) & ~255)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+
+    def __call__(self, q: torch.Tensor, kv_cache: torch.Tensor, seq_lens: torch.Tensor,
+                 qo_indptr: torch.Tensor, block_tables: torch.Tensor, sm_scale: float,
+                 kv_scale: float = 1.0, stream=None):
+        """block_tables: [W, B, width] int32 (W = 1 unsharded).  Returns (out, lse)."""
+        if self.W == 1:
+            mla.plan_rows(seq_lens, qo_indptr, self.T, block_tables[0], self.num_blocks,
+                          self.block_size, self.sp_stride, row_len=self.row_len,
+                          row_req=self.row_req, subpage_table=self.subpage[0], stream=stream)
+            mla.decode_verify(q, kv_cache, qo_indptr, self.row_len, self.subpage[0], self.P,
+                              self.S, self.max_qlen, sm_scale, kv_scale, out=self.out,
+                              lse=self.lse, workspace=self.workspace, stream=stream)
+            return self.out, self.lse
+        mla.plan_rows(seq_lens, qo_indptr, self.T, row_len=self.row_len, row_req=self.row_req,
+                      stream=stream)
+        for r in range(self.W):
+            mla.shard_row_view(qo_indptr, self.row_len, self.W, r, 1, block_tables[r],
+                               self.num_blocks, self.block_size, self.sp_stride,
+                               row_len_local=self.row_len_local[r],
+                               subpage_table=self.subpage[r], stream=stream)
+            mla.decode_verify(q, kv_cache, qo_indptr, self.row_len_local[r], self.subpage[r],
+                              self.P, self.S, self.max_qlen, sm_scale, kv_scale,
+                              out=self.part_out[r], lse=self.part_lse[r],
+                              workspace=self.workspace, stream=stream)
+        mla.merge_states(self.part_out, self.part_lse, out=self.out, lse=self.lse, stream=stream)
+        return self.out, self.lse
+
+
+def step_for_workload(wl, device="cuda", num_segments: Optional[int] = None) -> VerifyStep:
+    """A VerifyStep sized for a ``workloads.Workload``."""
+    return VerifyStep(num_reqs=wl.num_reqs, num_rows=wl.num_rows, num_heads=wl.num_heads,
+                      max_qlen=int(wl.qlens.max()), block_size=wl.block_size,
+                      num_blocks=wl.num_blocks, block_table_width=wl.block_tables.shape[2],
+                      max_kv_len=wl.max_kv_len,
+                      num_segments=wl.num_segments if num_segments is None else num_segments,
+                      world_size=wl.world_size, kv_fp8=(wl.kv_dtype == "fp8"), device=device)
+
+
+def device_inputs(wl, device="cuda"):
+    """Copies a workload's inputs to the device: (q, kv, seq_lens, qo_indptr, block_tables)."""
+    dev = torch.device(device)
+    q = wl.q.to(dev, non_blocking=True)
+    kv = wl.kv.to(dev, non_blocking=True)
+    seq = torch.as_tensor(wl.seq_lens, dtype=torch.int32).to(dev)
+    ind = torch.as_tensor(wl.qo_indptr, dtype=torch.int32).to(dev)
+    bt = torch.as_tensor(wl.block_tables, dtype=torch.int32).to(dev)
+    return q, kv, seq, ind, bt

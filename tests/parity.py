@@ -1,0 +1,76 @@
+"""Shared parity machinery: run a workload through the C ABI, compute the
+oracle on the same host bytes, compare with the stated tolerances.
+
+Tolerances (the stated bar for this path): per (row, head) the output error
+normalised by the row's scale, max_d |out - ref| / max_d |ref|, must be
+<= 1e-2, and the natural-log LSE must agree to 1e-3 absolute.  Indexing
+(row plan, shard view, sub-page tables) must be bit-exact.
+"""
+import numpy as np
+import torch
+
+import oracle
+
+OUT_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+def rowwise_errors(out_gpu, lse_gpu, out_ref, lse_ref):
+    """out_* [..., 512], lse_* [...] -> (normalised output error [...], lse error [...])."""
+    og = out_gpu.float().cpu().numpy().astype(np.float64) if torch.is_tensor(out_gpu) else out_gpu
+    lg = lse_gpu.float().cpu().numpy().astype(np.float64) if torch.is_tensor(lse_gpu) else lse_gpu
+    scale = np.maximum(np.abs(out_ref).max(axis=-1), 1e-30)
+    err = np.abs(og - out_ref).max(axis=-1) / scale
+    both_inf = np.isneginf(lg) & np.isneginf(lse_ref)
+    with np.errstate(invalid="ignore"):
+        lerr = np.where(both_inf, 0.0, np.abs(lg - lse_ref))
+    # an empty row must be exactly zero with lse = -inf
+    empty = np.isneginf(lse_ref)
+    err = np.where(empty, np.abs(og).max(axis=-1), err)
+    return err, lerr
+
+
+def assert_close(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
+    err, lerr = rowwise_errors(out_gpu, lse_gpu, out_ref, lse_ref)
+    assert np.isfinite(err).all() and np.isfinite(lerr).all(), f"{what}: non-finite result"
+    assert err.max() <= OUT_TOL, f"{what}: normalised output error {err.max():.3e} > {OUT_TOL}"
+    assert lerr.max() <= LSE_TOL, f"{what}: lse error {lerr.max():.3e} > {LSE_TOL}"
+    return float(err.max()), float(lerr.max())
+
+
+def oracle_reference(wl, sel=None):
+    """Oracle (out, lse) of a workload; sel = [n, 2] (row, head) pairs or None."""
+    q = wl.q_bits()
+    kv = wl.kv_host()
+    row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
+    if wl.world_size == 1:
+        return oracle.attention(wl.qo_indptr, row_len, q, kv, wl.kv_scale, wl.sm_scale,
+                                wl.block_tables[0], wl.block_size, sel=sel)
+    out, lse, _, _ = oracle.sharded_attention(wl.qo_indptr, row_len, q, kv, wl.kv_scale,
+                                              wl.sm_scale, wl.block_tables, wl.block_size,
+                                              wl.world_size, sel=sel)
+    return out, lse
+
+
+def sample_pairs(wl, n, seed=0):
+    """n (row, head) pairs: every request's last row and first row, plus random ones."""
+    rng = np.random.default_rng(seed)
+    ind = wl.qo_indptr
+    rows = []
+    for b in range(wl.num_reqs):
+        rows += [ind[b], ind[b + 1] - 1]
+    rows = np.array(rows)
+    pick = rng.choice(rows, size=min(n // 2, rows.size), replace=False)
+    extra = rng.integers(0, wl.num_rows, n - pick.size)
+    r = np.concatenate([pick, extra])
+    h = rng.integers(0, wl.num_heads, r.size)
+    return np.stack([r, h], axis=1).astype(np.int32)
+
+
+def run_gpu(wl, num_segments=None, device="cuda"):
+    from mla_decode_speculative_gb300 import runner
+    step = runner.step_for_workload(wl, device, num_segments)
+    q, kv, seq, ind, bt = runner.device_inputs(wl, device)
+    out, lse = step(q, kv, seq, ind, bt, wl.sm_scale, wl.kv_scale)
+    torch.cuda.synchronize()
+    return out, lse, step

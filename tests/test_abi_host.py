@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/mla_gb300.h declares, and rejects bad
+arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_decode_speculative_gb300 import build, mla
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "mla_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return mla.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mla_plan_rows", "mla_shard_row_view", "mla_decode_verify", "mla_merge_segments",
+              "mla_decode_verify_workspace", "mla_get_device_error", "mla_page_size"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in declared_functions():
+        assert hasattr(L, n), f"{n} declared in mla_gb300.h but not exported"
+    assert L.mla_abi_version() == 1
+
+
+def test_page_size_matches_rule(L):
+    for bs, p in [(16, 16), (64, 64), (256, 128), (96, 32), (1, 1), (0, -1), (-8, -1), (1000, 8)]:
+        assert L.mla_page_size(bs) == p
+
+
+def test_status_strings(L):
+    assert mla.lib().mla_status_string(0) == b"MLA_OK"
+    assert mla.lib().mla_status_string(2) == b"MLA_ERR_UNSUPPORTED"
+
+
+def test_host_validation_without_cuda(L):
+    vp = ctypes.c_void_p
+    # shard view: interleave != 1 is unsupported, checked before anything else
+    st = L.mla_shard_row_view(1, 1, vp(8), vp(8), 4, 0, 2, vp(8), None, 0, 0, 0, None, 0, None)
+    assert st == mla.MLA_ERR_UNSUPPORTED
+    assert b"interleave" in L.mla_last_error_string()
+    st = L.mla_shard_row_view(1, 1, vp(8), vp(8), 4, 4, 1, vp(8), None, 0, 0, 0, None, 0, None)
+    assert st == mla.MLA_ERR_INVALID_ARG
+    # plan rows: negative sizes, non-positive block size
+    assert L.mla_plan_rows(-1, 1, vp(8), vp(8), vp(8), vp(8), None, 0, 0, 0, None, 0, None) == 1
+    assert L.mla_plan_rows(1, 1, vp(8), vp(8), vp(8), vp(8), vp(8), 4, 4, 0, vp(8), 4, None) == 1
+    # decode: page size 4 unsupported, bad dtype, missing workspace
+    a = mla.DecodeArgs()
+    a.num_reqs, a.num_rows, a.num_heads, a.max_qlen = 1, 1, 16, 1
+    a.kv_dtype, a.sm_scale, a.kv_scale = 0, 0.07, 1.0
+    a.q = a.kv_cache = a.qo_indptr = a.row_len = a.subpage_table = a.out = a.lse = 256
+    a.num_cache_rows, a.subpage_stride, a.page_size, a.num_segments = 64, 4, 4, 1
+    assert L.mla_decode_verify(ctypes.byref(a), None, 0, None) == mla.MLA_ERR_UNSUPPORTED
+    a.page_size = 16
+    a.kv_dtype = 7
+    assert L.mla_decode_verify(ctypes.byref(a), None, 0, None) == mla.MLA_ERR_UNSUPPORTED
+    a.kv_dtype = 0
+    a.num_segments = 4
+    assert L.mla_decode_verify_workspace(ctypes.byref(a)) > 0
+    assert L.mla_decode_verify(ctypes.byref(a), None, 0, None) == mla.MLA_ERR_WORKSPACE
+    a.q = 258  # misaligned
+    assert L.mla_decode_verify(ctypes.byref(a), None, 0, None) == mla.MLA_ERR_INVALID_ARG
+    # merge: unknown mode
+    m = mla.MergeArgs()
+    m.mode, m.num_rows, m.num_heads, m.num_parts = 9, 1, 1, 1
+    m.out = m.lse = 256
+    assert L.mla_merge_segments(ctypes.byref(m), None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_workspace_size_formula(L):
+    a = mla.DecodeArgs()
+    a.num_rows, a.num_heads, a.num_segments = 128, 16, 16
+    items = 128 * 16 * 16
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert L.mla_decode_verify_workspace(ctypes.byref(a)) == r256(items * 2048) + 2 * r256(items * 4)
+    a.num_segments = 1
+    assert L.mla_decode_verify_workspace(ctypes.byref(a)) == 0

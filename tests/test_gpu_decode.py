@@ -1,0 +1,144 @@
+"""Decode / causal verify through the C ABI against the float64 oracle.
+
+Small workloads are compared on every (row, head); full-size configured
+workloads (in the launch configuration the benchmark times) on sampled pairs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import assert_close, oracle_reference, run_gpu, sample_pairs
+from mla_decode_speculative_gb300 import mla, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_check(wl, what, num_segments=None):
+    out, lse, _ = run_gpu(wl, num_segments)
+    assert mla.get_device_error() == 0
+    ref_o, ref_l = oracle_reference(wl)
+    return assert_close(out, lse, ref_o, ref_l, what)
+
+
+def _sampled_check(wl, n, what, seed=0):
+    out, lse, _ = run_gpu(wl)
+    assert mla.get_device_error() == 0
+    sel = sample_pairs(wl, n, seed)
+    ref_o, ref_l = oracle_reference(wl, sel)
+    o = out[sel[:, 0], sel[:, 1]]
+    l = lse[sel[:, 0], sel[:, 1]]
+    return assert_close(o, l, ref_o, ref_l, what)
+
+
+# ------------------------------------------------------------------ small, every pair
+
+def test_decode_qlen1_bf16_full():
+    _full_check(workloads.decode_qlen1_bf16(), "qlen=1 bf16 decode, batch 2, L 256, block 16")
+
+
+@pytest.mark.parametrize("S", [1, 3, 16])
+def test_verify_mtp4_small_every_pair(S):
+    wl = workloads.verify_mtp4_bf16(seed=1, batch=5, lo=130, hi=1500, num_segments=S)
+    _full_check(wl, f"verify qlen=4, S={S}")
+
+
+def test_fp8_small_every_pair():
+    wl = workloads.fp8_mixed_qlen(seed=2, batch=7, lo=100, hi=2500, num_segments=3)
+    _full_check(wl, "fp8 e4m3 verify, qlen 1-3, 12 heads")
+
+
+def test_dcp_small_every_pair():
+    wl = workloads.dcp8_verify_bf16(seed=3, batch=3, context=3000, world_size=8, num_segments=2)
+    _full_check(wl, "8-way round-robin sharded verify")
+
+
+@pytest.mark.parametrize("block_size", [16, 64, 256])
+def test_block_sizes_and_subpages(block_size):
+    rng = np.random.default_rng(block_size)
+    L = rng.integers(5, 900, 6)
+    wl = workloads.make_workload(f"bs{block_size}", L, np.minimum(L, 4), 16, block_size,
+                                 num_segments=2, seed=block_size)
+    _full_check(wl, f"block_size {block_size}")
+
+
+def test_many_rows_per_request_and_short_windows():
+    # 32 heads x qlen 6 = 192 rows (three 64-row blocks); qlen == seq_len rows
+    wl = workloads.make_workload("wide", [6, 300, 77], [6, 6, 5], 32, 16, num_segments=2, seed=9)
+    _full_check(wl, "192 rows per request, window of 1 token")
+
+
+def test_single_token_and_tiny_lengths():
+    wl = workloads.make_workload("tiny", [1, 2, 3, 129, 128], [1, 2, 1, 1, 3], 16, 16,
+                                 num_segments=4, seed=4)
+    _full_check(wl, "tiny windows")
+
+
+def test_dcp_windows_shorter_than_world():
+    # seq_len < W: several shards see no token for some rows
+    wl = workloads.make_workload("dcp_short", [3, 5, 9], [3, 2, 4], 16, 16, world_size=8,
+                                 num_segments=1, seed=5, max_kv_len=2)
+    _full_check(wl, "windows shorter than the shard count")
+
+
+def test_nan_in_unused_cache_slots_is_never_read():
+    wl = workloads.make_workload("nan_slots", [70, 200, 33], [3, 4, 2], 16, 64, num_segments=2,
+                                 seed=6)
+    # poison every cache row no request can see
+    visible = np.zeros(wl.kv_rows, bool)
+    for b in range(wl.num_reqs):
+        for j in range(int(wl.seq_lens[b])):
+            blk = wl.block_tables[0, b, j // wl.block_size]
+            visible[blk * wl.block_size + j % wl.block_size] = True
+    kv = wl.kv.clone()
+    kv[torch.as_tensor(~visible)] = float("nan")
+    wl.kv = kv
+    _full_check(wl, "NaN in invisible cache rows")
+
+
+def test_segment_partials_match_oracle():
+    wl = workloads.verify_mtp4_bf16(seed=7, batch=3, lo=300, hi=1300, num_segments=5)
+    out, lse, step = run_gpu(wl)
+    segm_out, segm_max, segm_sum = mla.workspace_views(step.workspace, wl.num_rows, wl.num_heads, 5)
+    row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
+    acc, mx, sm = oracle.segment_partials(wl.qo_indptr, row_len, wl.q_bits(), wl.kv_host(), 1.0,
+                                          wl.sm_scale, wl.block_tables[0], wl.block_size, 5,
+                                          oracle.page_size(wl.block_size))
+    gm, gs = segm_max.cpu().numpy(), segm_sum.cpu().numpy()
+    go = segm_out.cpu().numpy()
+    live = sm > 0
+    assert (np.isneginf(gm) == ~live).all(), "GPU and oracle disagree on which segments are empty"
+    # normalised segment output and segment LSE (invariant to the reference max)
+    norm_ref = acc[live] / sm[live][:, None]
+    norm_gpu = go[live] / gs[live][:, None]
+    scale = np.abs(norm_ref).max(axis=-1)
+    assert (np.abs(norm_gpu - norm_ref).max(axis=-1) / scale).max() <= 1e-2
+    lse2_ref = mx[live] + np.log2(sm[live])
+    lse2_gpu = gm[live] + np.log2(gs[live])
+    assert np.abs(lse2_gpu - lse2_ref).max() * math.log(2) <= 1e-3
+
+
+def test_static_bound_does_not_change_results():
+    wl = workloads.verify_mtp4_bf16(seed=8, batch=4, lo=100, hi=700, num_segments=4)
+    out1, lse1, _ = run_gpu(wl)
+    wl2 = workloads.verify_mtp4_bf16(seed=8, batch=4, lo=100, hi=700, num_segments=4)
+    wl2.max_kv_len = 4096  # wider sub-page table, same data
+    out2, lse2, _ = run_gpu(wl2)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+# ------------------------------------------------------------------ full-size, sampled
+
+def test_verify_mtp4_full_size_sampled():
+    _sampled_check(workloads.verify_mtp4_bf16(), 96, "verify qlen=4 batch 32 L 1k-8k S=16")
+
+
+def test_fp8_full_size_sampled():
+    _sampled_check(workloads.fp8_mixed_qlen(), 96, "fp8 batch 64 L 512-32k")
+
+
+def test_dcp8_full_size_sampled():
+    wl = workloads.dcp8_verify_bf16(device="cuda")
+    _sampled_check(wl, 24, "dcp8 batch 16 context 128k")
