@@ -259,6 +259,15 @@ def source_hash() -> str:
     return h.hexdigest()
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The slowest rank's value (max all-reduce); the identity on one process."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -329,8 +338,11 @@ def main():
         torch.cuda.synchronize()
         return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
-    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
-                           else local)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
     sampler.start()
     time.sleep(0.3)
     with torch.cuda.stream(stream):
@@ -348,11 +360,7 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    mean_ms = float(np.mean(step_ms))
-    if dist:
-        tt = torch.tensor([mean_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        mean_ms = float(tt.item())
+    mean_ms = max_over_ranks(float(np.mean(step_ms)), dist, dev)
     dec_ms = None
     if dgraph is not None:
         dec_ms = float(np.mean(timed(dgraph, max(20, min(args.steps, 500)))))
@@ -390,11 +398,8 @@ def main():
                 if k >= 3:
                     e_ev[k - 3].record(stream)
                 stream.synchronize()
-        e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(s_ev, e_ev)]))
-        if dist:
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(s_ev, e_ev)])),
+                                dist, dev)
         bi = sum(x.numel() * x.element_size() for x in (h_q, h_seq, h_ind, h_bt))
         bo = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
         e2e = {"value": world * kv_bytes(wl) / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
