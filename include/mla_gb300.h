@@ -154,7 +154,7 @@ typedef struct mla_decode_args {
   const int32_t *subpage_table;  /* [B, subpage_stride] sub-page ids (mla_plan_rows) */
   int subpage_stride;
   int page_size;         /* P = mla_page_size(block_size); 8 <= P <= 128 */
-  int num_segments;      /* S >= 1 split-K segments per request */
+  int num_segments;      /* S split-K segments per request, 1 <= S <= 1024 */
   void *out;             /* [T, H, 512] bf16 output */
   float *lse;            /* [T, H] natural-log LSE (-inf for a row with no tokens) */
   int flags;             /* bitwise OR of mla_decode_flags (0 = default) */
@@ -168,9 +168,12 @@ typedef enum mla_decode_flags {
   MLA_DECODE_SKIP_MERGE = 1
 } mla_decode_flags;
 
-/* Workspace bytes mla_decode_verify needs for `a` (0 when num_segments == 1):
- *   segm_out [T, H, S, 512] float32, segm_max [T, H, S], segm_sum [T, H, S],
- * each region starting on a 256-byte boundary, in that order.  Host only. */
+/* Workspace bytes mla_decode_verify needs for `a`.  Layout, each region
+ * starting on a 256-byte boundary, in this order:
+ *   segm_out [T, H, S, 512] float32, segm_max [T, H, S], segm_sum [T, H, S]
+ *   (these three only when num_segments > 1), then 256 bytes of scheduler
+ *   state (a work counter the call zeroes on the stream before its kernel).
+ * Host only. */
 size_t mla_decode_verify_workspace(const mla_decode_args *a);
 
 /* Absorbed-form MLA decode / causal verify over the paged latent cache.
@@ -209,7 +212,7 @@ typedef struct mla_merge_args {
   int mode;        /* mla_merge_mode */
   int num_rows;    /* T */
   int num_heads;   /* H */
-  int num_parts;   /* S segments or W shards, >= 1 */
+  int num_parts;   /* S segments or W shards, 1 <= num_parts <= 1024 */
   /* MLA_MERGE_SEGMENTS: [T, H, S, 512] float32 unnormalised partial outputs,
    * [T, H, S] base-2 maxima and exp2 sums; a part with max = -inf is empty
    * and its output is never read. */
@@ -234,6 +237,29 @@ typedef struct mla_merge_args {
  *   lse = M + ln sum_r w_r.
  * All parts empty: out = 0, lse = -inf.  out is rounded to bf16 (RNE). */
 mla_status mla_merge_segments(const mla_merge_args *a, mla_stream_t stream);
+
+/* The same decode / verify as mla_decode_verify, for callers that cannot
+ * allocate device memory where they make the call -- code running under
+ * CUDA-graph capture (cudaMalloc is not allowed there), serving runtimes that
+ * reserve all device memory at start-up and forbid allocation on the request
+ * path, and plain C or plugin hosts that hold no device allocator (for them a
+ * cudaMalloc would also synchronise the device mid-step).  The pages have no
+ * counterpart: this is a deployment convenience of this library.
+ * The scratch mla_decode_verify would take from the caller's workspace is
+ * instead a fixed array of MLA_STATIC_SCRATCH_BYTES in the library's device
+ * memory, which every GPU that loads the library holds until the process
+ * exits.  The call allocates nothing (no cudaMalloc / cudaFree, no allocating
+ * library routine).  Problems whose mla_decode_verify_workspace(a) exceeds the
+ * array are rejected with MLA_ERR_WORKSPACE before anything is launched.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array per device and leaves its
+ * contents behind (the work counter in it is zeroed on the stream by each
+ * call): calls whose work overlaps on the GPU -- on different streams, or from
+ * different host threads -- race on it and must be serialised by the caller.
+ * Arguments, outputs and errors are otherwise those of mla_decode_verify. */
+#define MLA_STATIC_SCRATCH_BYTES (80u * 1024u * 1024u)
+mla_status mla_decode_verify_noalloc(const mla_decode_args *a, mla_stream_t stream);
 
 /* Synchronises `stream`, returns the first device error code recorded on the
  * current device since the last call (MLA_DEV_OK if none) in *code_out, and

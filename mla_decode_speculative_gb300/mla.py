@@ -68,7 +68,7 @@ class MergeArgs(ctypes.Structure):
 _lib = None
 _lock = threading.Lock()
 EXPORTS = ("mla_page_size", "mla_plan_rows", "mla_shard_row_view", "mla_decode_verify_workspace",
-           "mla_decode_verify", "mla_merge_segments", "mla_get_device_error",
+           "mla_decode_verify", "mla_decode_verify_noalloc", "mla_merge_segments", "mla_get_device_error",
            "mla_last_error_string", "mla_status_string", "mla_abi_version")
 
 
@@ -100,6 +100,8 @@ def lib():
         L.mla_decode_verify_workspace.restype = ctypes.c_size_t
         L.mla_decode_verify.argtypes = [ctypes.POINTER(DecodeArgs), vp, ctypes.c_size_t, vp]
         L.mla_decode_verify.restype = c_int
+        L.mla_decode_verify_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), vp]
+        L.mla_decode_verify_noalloc.restype = c_int
         L.mla_merge_segments.argtypes = [ctypes.POINTER(MergeArgs), vp]
         L.mla_merge_segments.restype = c_int
         L.mla_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
@@ -248,6 +250,28 @@ def decode_verify(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_, nu
     _check(lib().mla_decode_verify(ctypes.byref(a), ws_ptr, need, _stream(stream)),
            "mla_decode_verify")
     return out, lse, workspace
+
+
+STATIC_SCRATCH_BYTES = 80 * 1024 * 1024
+
+
+def decode_verify_noalloc(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_,
+                          num_segments, max_qlen, sm_scale, kv_scale=1.0, out=None, lse=None,
+                          stream=None):
+    """mla_decode_verify_noalloc: the library's own static device scratch instead of a
+    caller workspace, for callers that cannot allocate device memory at the call (under
+    graph capture, fixed-budget serving runtimes, allocator-less C hosts).  Calls that
+    overlap on the GPU share that scratch and must be serialised.  Returns (out, lse)."""
+    T, H, _ = q.shape
+    if out is None:
+        out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    a = make_decode_args(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_,
+                         num_segments, max_qlen, sm_scale, kv_scale, out, lse)
+    _check(lib().mla_decode_verify_noalloc(ctypes.byref(a), _stream(stream)),
+           "mla_decode_verify_noalloc")
+    return out, lse
 
 
 def workspace_views(workspace: torch.Tensor, num_rows: int, num_heads: int, num_segments: int):
