@@ -430,8 +430,11 @@ def main():
 
     kvb = kv_bytes(wl)
     value = world * kvb / (mean_ms * 1e-3) / 1e9
-    launches_per_step = (4 if wl.world_size == 1 and wl.num_segments > 1 else
-                         3 if wl.world_size == 1 else 1 + wl.world_size * 4 + 1)
+    # plan (1) + decode (1) + segment merge (1 if S > 1); sharded: plan + W x
+    # (shard view + decode + segment merge) + state merge
+    per_decode = 2 if wl.num_segments > 1 else 1
+    launches_per_step = (1 + per_decode if wl.world_size == 1 else
+                         1 + wl.world_size * (1 + per_decode) + 1)
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

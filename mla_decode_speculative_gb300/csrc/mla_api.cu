@@ -42,21 +42,62 @@ __device__ __forceinline__ int find_request(const int32_t *ind, int B, int r) {
   return lo;
 }
 
-// Row plan: row t of request b sees global positions [0, L_b - qlen_b + t]
-// [vLLM #51705 digest, 实现拆解 2].
-__global__ void plan_rows_kernel(int B, int T, const int32_t *seq_lens, const int32_t *ind,
-                                 int32_t *row_len, int32_t *row_req, int *err) {
+// Sub-page row of one request [vLLM #51705 digest, 实现拆解 3]: local page p
+// is block_table[b][p / R] * R + p % R (R = block_size / P) for the pages
+// that hold `len` tokens, -1 after that.  Run by one block.
+__device__ void subpage_row(int b, int len, const int32_t *bt, int bt_stride, int num_blocks,
+                            int block_size, int P, int32_t *sp, int sp_stride, int *err) {
+  int pages = (len + P - 1) / P;
+  if (pages > sp_stride) {
+    if (threadIdx.x == 0) dev_error(err, MLA_DEV_LEN_BOUND);
+    pages = sp_stride;
+  }
+  const int R = block_size / P;
+  int32_t *row = sp + static_cast<int64_t>(b) * sp_stride;
+  for (int pg = threadIdx.x; pg < sp_stride; pg += blockDim.x) {
+    int32_t v = -1;
+    if (pg < pages) {
+      const int bi = pg / R;
+      const int blk = bi < bt_stride ? bt[static_cast<int64_t>(b) * bt_stride + bi] : -1;
+      if (blk < 0 || blk >= num_blocks) dev_error(err, MLA_DEV_BAD_BLOCK_ID);
+      else v = blk * R + pg % R;
+    }
+    row[pg] = v;
+  }
+}
+
+struct TableArgs {
+  const int32_t *bt;
+  int bt_stride, num_blocks, block_size, P;
+  int32_t *sp;
+  int sp_stride;
+};
+
+// Row plan [vLLM #51705 digest, 实现拆解 2]: row t of request b sees global
+// positions [0, L_b - qlen_b + t].  Blocks [0, row_blocks) write the rows;
+// blocks row_blocks + b expand request b's block table (its longest row sees
+// all L_b tokens) when a table is given.
+__global__ void plan_kernel(int B, int T, const int32_t *seq_lens, const int32_t *ind,
+                            int32_t *row_len, int32_t *row_req, TableArgs tab, int row_blocks,
+                            int *err) {
   const int total = ind[B];
   const bool ind_ok = ind[0] == 0 && total >= 0 && total <= T;
-  const int stride = gridDim.x * blockDim.x;
+  if (blockIdx.x >= row_blocks) {
+    const int b = blockIdx.x - row_blocks;
+    const int qlen = ind[b + 1] - ind[b];
+    const int L = seq_lens[b];
+    const int len = (ind_ok && qlen >= 1 && qlen <= L) ? L : 0;
+    subpage_row(b, len, tab.bt, tab.bt_stride, tab.num_blocks, tab.block_size, tab.P, tab.sp,
+                tab.sp_stride, err);
+    return;
+  }
+  const int stride = row_blocks * blockDim.x;
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += stride) {
     const int qlen = ind[b + 1] - ind[b];
     if (qlen < 0) dev_error(err, MLA_DEV_BAD_INDPTR);
     else if (qlen == 0 || qlen > seq_lens[b]) dev_error(err, MLA_DEV_BAD_QLEN);
   }
-  if (!ind_ok) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) dev_error(err, MLA_DEV_BAD_INDPTR);
-  }
+  if (!ind_ok && blockIdx.x == 0 && threadIdx.x == 0) dev_error(err, MLA_DEV_BAD_INDPTR);
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < T; r += stride) {
     if (!ind_ok || r >= total) {
       row_len[r] = 0;
@@ -73,52 +114,28 @@ __global__ void plan_rows_kernel(int B, int T, const int32_t *seq_lens, const in
   }
 }
 
-// Shard row view: per-row shard-local count from the row's global window.
-__global__ void shard_rows_kernel(int B, int T, const int32_t *ind, const int32_t *row_len_global,
-                                  int W, int rank, int32_t *row_len_local, int *err) {
+// Shard row view: per-row shard-local count from the row's global window;
+// blocks row_blocks + b expand the shard's table for request b, sized by its
+// longest shard-local row.
+__global__ void shard_kernel(int B, int T, const int32_t *ind, const int32_t *row_len_global,
+                             int W, int rank, int32_t *row_len_local, TableArgs tab,
+                             int row_blocks, int *err) {
   const int total = ind[B];
   const bool ind_ok = ind[0] == 0 && total >= 0 && total <= T;
-  if (!ind_ok && blockIdx.x == 0 && threadIdx.x == 0) dev_error(err, MLA_DEV_BAD_INDPTR);
-  const int stride = gridDim.x * blockDim.x;
-  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < T; r += stride) {
-    row_len_local[r] = (ind_ok && r < total) ? rr_count(row_len_global[r], W, rank) : 0;
-  }
-}
-
-// Sub-page table [vLLM #51705 digest, 实现拆解 3]: local page p of request b is
-// block_table[b][p / R] * R + p % R (R = block_size / P) for the pages that
-// hold the request's longest row, -1 after that.
-__global__ void subpage_table_kernel(int B, const int32_t *ind, const int32_t *row_len,
-                                     const int32_t *bt, int bt_stride, int num_blocks,
-                                     int block_size, int P, int32_t *sp, int sp_stride, int *err) {
-  const int b = blockIdx.x;
-  if (b >= B) return;
-  __shared__ int s_pages;
-  if (threadIdx.x == 0) {
+  if (blockIdx.x >= row_blocks) {
+    const int b = blockIdx.x - row_blocks;
     int len = 0;
     const int r0 = ind[b], r1 = ind[b + 1];
-    if (r0 >= 0 && r1 >= r0)
-      for (int r = r0; r < r1; ++r) len = max(len, row_len[r]);
-    int pages = (len + P - 1) / P;
-    if (pages > sp_stride) {
-      dev_error(err, MLA_DEV_LEN_BOUND);
-      pages = sp_stride;
-    }
-    s_pages = pages;
+    if (ind_ok && r0 >= 0 && r1 >= r0 && r1 <= T)
+      for (int r = r0; r < r1; ++r) len = max(len, rr_count(row_len_global[r], W, rank));
+    subpage_row(b, len, tab.bt, tab.bt_stride, tab.num_blocks, tab.block_size, tab.P, tab.sp,
+                tab.sp_stride, err);
+    return;
   }
-  __syncthreads();
-  const int pages = s_pages;
-  const int R = block_size / P;
-  int32_t *row = sp + static_cast<int64_t>(b) * sp_stride;
-  for (int pg = threadIdx.x; pg < sp_stride; pg += blockDim.x) {
-    int32_t v = -1;
-    if (pg < pages) {
-      const int bi = pg / R;
-      const int blk = bi < bt_stride ? bt[static_cast<int64_t>(b) * bt_stride + bi] : -1;
-      if (blk < 0 || blk >= num_blocks) dev_error(err, MLA_DEV_BAD_BLOCK_ID);
-      else v = blk * R + pg % R;
-    }
-    row[pg] = v;
+  if (!ind_ok && blockIdx.x == 0 && threadIdx.x == 0) dev_error(err, MLA_DEV_BAD_INDPTR);
+  const int stride = row_blocks * blockDim.x;
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < T; r += stride) {
+    row_len_local[r] = (ind_ok && r < total) ? rr_count(row_len_global[r], W, rank) : 0;
   }
 }
 
@@ -196,30 +213,45 @@ mla_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType 
 }
 
 mla_status launch_plan_rows(int B, int T, const int32_t *seq_lens, const int32_t *ind,
-                            int32_t *row_len, int32_t *row_req, int *err, cudaStream_t stream) {
-  const int n = T > B ? T : B;
-  plan_rows_kernel<<<grid_for(n, 256), 256, 0, stream>>>(B, T, seq_lens, ind, row_len, row_req, err);
+                            int32_t *row_len, int32_t *row_req, const TableLaunch &t,
+                            int *err, cudaStream_t stream) {
+  const int row_blocks = grid_for(T > B ? T : B, 256);
+  TableArgs tab{t.block_table, t.bt_stride, t.num_blocks, t.block_size, t.page_size,
+                t.subpage_table, t.sp_stride};
+  const int blocks = row_blocks + (t.block_table != nullptr ? B : 0);
+  plan_kernel<<<blocks, 256, 0, stream>>>(B, T, seq_lens, ind, row_len, row_req, tab, row_blocks, err);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan_rows launch");
 }
 
 mla_status launch_shard_rows(int B, int T, const int32_t *ind, const int32_t *row_len_global,
-                             int W, int rank, int32_t *row_len_local, int *err,
-                             cudaStream_t stream) {
-  shard_rows_kernel<<<grid_for(T, 256), 256, 0, stream>>>(B, T, ind, row_len_global, W, rank,
-                                                           row_len_local, err);
+                             int W, int rank, int32_t *row_len_local, const TableLaunch &t,
+                             int *err, cudaStream_t stream) {
+  const int row_blocks = grid_for(T, 256);
+  TableArgs tab{t.block_table, t.bt_stride, t.num_blocks, t.block_size, t.page_size,
+                t.subpage_table, t.sp_stride};
+  const int blocks = row_blocks + (t.block_table != nullptr ? B : 0);
+  shard_kernel<<<blocks, 256, 0, stream>>>(B, T, ind, row_len_global, W, rank, row_len_local, tab,
+                                           row_blocks, err);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "shard_row_view launch");
 }
 
-mla_status launch_subpage_table(int B, const int32_t *ind, const int32_t *row_len,
-                                const int32_t *bt, int bt_stride, int num_blocks, int block_size,
-                                int P, int32_t *sp, int sp_stride, int *err, cudaStream_t stream) {
-  if (B == 0) return MLA_OK;
-  subpage_table_kernel<<<B, 128, 0, stream>>>(B, ind, row_len, bt, bt_stride, num_blocks,
-                                              block_size, P, sp, sp_stride, err);
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "subpage_table launch");
+WorkspaceLayout decode_workspace_layout(const mla_decode_args &a) {
+  WorkspaceLayout l{};
+  size_t off = 0;
+  if (a.num_segments > 1) {
+    const size_t items = static_cast<size_t>(a.num_rows) * a.num_heads * a.num_segments;
+    l.segm_out = off;
+    off += align256(items * 512 * sizeof(float));
+    l.segm_max = off;
+    off += align256(items * sizeof(float));
+    l.segm_sum = off;
+    off += align256(items * sizeof(float));
+  }
+  l.sched = off;
+  l.total = off + 256;
+  return l;
 }
 
 }  // namespace mla
@@ -291,10 +323,9 @@ mla_status mla_plan_rows(int num_reqs, int num_rows, const int32_t *seq_lens,
   int *err = device_error_word();
   if (err == nullptr) return MLA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  mla_status st = launch_plan_rows(num_reqs, num_rows, seq_lens, qo_indptr, row_len, row_req, err, s);
-  if (st != MLA_OK || block_table == nullptr) return st;
-  return launch_subpage_table(num_reqs, qo_indptr, row_len, block_table, block_table_stride,
-                              num_blocks, block_size, P, subpage_table, subpage_stride, err, s);
+  TableLaunch t{block_table, block_table_stride, num_blocks, block_size, P, subpage_table,
+                subpage_stride};
+  return launch_plan_rows(num_reqs, num_rows, seq_lens, qo_indptr, row_len, row_req, t, err, s);
 }
 
 mla_status mla_shard_row_view(int num_reqs, int num_rows, const int32_t *qo_indptr,
@@ -324,11 +355,10 @@ mla_status mla_shard_row_view(int num_reqs, int num_rows, const int32_t *qo_indp
   int *err = device_error_word();
   if (err == nullptr) return MLA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  mla_status st = launch_shard_rows(num_reqs, num_rows, qo_indptr, row_len_global, world_size,
-                                    rank, row_len_local, err, s);
-  if (st != MLA_OK || block_table == nullptr) return st;
-  return launch_subpage_table(num_reqs, qo_indptr, row_len_local, block_table, block_table_stride,
-                              num_blocks, block_size, P, subpage_table, subpage_stride, err, s);
+  TableLaunch t{block_table, block_table_stride, num_blocks, block_size, P, subpage_table,
+                subpage_stride};
+  return launch_shard_rows(num_reqs, num_rows, qo_indptr, row_len_global, world_size, rank,
+                           row_len_local, t, err, s);
 }
 
 static mla_status check_decode_args(const mla_decode_args *a) {
@@ -356,10 +386,8 @@ static mla_status check_decode_args(const mla_decode_args *a) {
     set_error("mla_decode_verify: sizes overflow int32 indexing");
     return MLA_ERR_INVALID_ARG;
   }
-  if (a->num_segments > 65535 || a->num_reqs > 65535 ||
-      (static_cast<int64_t>(a->max_qlen) * a->num_heads + 63) / 64 > 65535) {
-    set_error("mla_decode_verify: grid too large (S=%d B=%d max_qlen*H=%lld)", a->num_segments,
-              a->num_reqs, (long long)a->max_qlen * a->num_heads);
+  if (a->num_segments > kMaxParts) {
+    set_error("mla_decode_verify: num_segments %d above the supported %d", a->num_segments, kMaxParts);
     return MLA_ERR_UNSUPPORTED;
   }
   if (a->q == nullptr || a->kv_cache == nullptr || a->qo_indptr == nullptr || a->row_len == nullptr ||
@@ -383,37 +411,36 @@ static mla_status check_decode_args(const mla_decode_args *a) {
 }
 
 size_t mla_decode_verify_workspace(const mla_decode_args *a) {
-  if (a == nullptr || a->num_segments <= 1 || a->num_rows < 1 || a->num_heads < 1) return 0;
-  const size_t items = static_cast<size_t>(a->num_rows) * a->num_heads * a->num_segments;
-  return align256(items * 512 * sizeof(float)) + 2 * align256(items * sizeof(float));
+  if (a == nullptr || a->num_rows < 1 || a->num_heads < 1 || a->num_segments < 1) return 0;
+  return decode_workspace_layout(*a).total;
 }
 
 mla_status mla_decode_verify(const mla_decode_args *a, void *workspace, size_t workspace_bytes,
                              mla_stream_t stream) {
   mla_status st = check_decode_args(a);
   if (st != MLA_OK) return st;
-  const size_t need = mla_decode_verify_workspace(a);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !is_aligned(workspace, 256))) {
+  const WorkspaceLayout lay = decode_workspace_layout(*a);
+  if (workspace == nullptr || workspace_bytes < lay.total || !is_aligned(workspace, 256)) {
     set_error("mla_decode_verify: workspace of %zu bytes (256-byte aligned) needed, got %zu at %p",
-              need, workspace_bytes, workspace);
+              lay.total, workspace_bytes, workspace);
     return MLA_ERR_WORKSPACE;
   }
   int *err = device_error_word();
   if (err == nullptr) return MLA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *w = static_cast<char *>(workspace);
   DecodeLaunch d{};
   d.a = a;
   d.err = err;
-  if (need > 0) {
-    const size_t items = static_cast<size_t>(a->num_rows) * a->num_heads * a->num_segments;
-    char *w = static_cast<char *>(workspace);
-    d.segm_out = reinterpret_cast<float *>(w);
-    d.segm_max = reinterpret_cast<float *>(w + align256(items * 512 * sizeof(float)));
-    d.segm_sum = reinterpret_cast<float *>(w + align256(items * 512 * sizeof(float)) +
-                                           align256(items * sizeof(float)));
+  d.sched = reinterpret_cast<int *>(w + lay.sched);
+  const bool partials = a->num_segments > 1;
+  if (partials) {
+    d.segm_out = reinterpret_cast<float *>(w + lay.segm_out);
+    d.segm_max = reinterpret_cast<float *>(w + lay.segm_max);
+    d.segm_sum = reinterpret_cast<float *>(w + lay.segm_sum);
   }
   st = launch_decode(d, s);
-  if (st != MLA_OK || need == 0 || (a->flags & MLA_DECODE_SKIP_MERGE)) return st;
+  if (st != MLA_OK || !partials || (a->flags & MLA_DECODE_SKIP_MERGE)) return st;
   MergeLaunch m{};
   m.mode = MLA_MERGE_SEGMENTS;
   m.num_rows = a->num_rows;
@@ -433,6 +460,10 @@ mla_status mla_merge_segments(const mla_merge_args *a, mla_stream_t stream) {
       a->out == nullptr || a->lse == nullptr) {
     set_error("mla_merge_segments: bad arguments");
     return MLA_ERR_INVALID_ARG;
+  }
+  if (a->num_parts > kMaxParts) {
+    set_error("mla_merge_segments: num_parts %d above the supported %d", a->num_parts, kMaxParts);
+    return MLA_ERR_UNSUPPORTED;
   }
   if (a->mode == MLA_MERGE_SEGMENTS) {
     if (a->segm_out == nullptr || a->segm_max == nullptr || a->segm_sum == nullptr ||

@@ -15,9 +15,11 @@
 //    rows of a request (heads x qlen) are decoded jointly against shared
 //    128-token KV tiles, so each latent row is read from HBM once per request
 //    (the pages replicate the request once per verify row).
-//  * Persistent CTAs, one per SM, walk the work items round-robin; the next
-//    item's Q and first tile are loaded while the current item's epilogue
-//    runs.  Every barrier phase follows one running tile counter.
+//  * Persistent CTAs, one per SM.  The producer warp claims items from an
+//    atomic counter (dynamic load balance) and publishes each decoded item,
+//    with its rows' visible lengths, through a 4-deep shared-memory work
+//    ring; the next item's Q and first tile are loaded while the current
+//    item's epilogue runs.  Every barrier phase follows one running counter.
 //  * Swapped operand order, so every UMMA is M = 128 and the O accumulator
 //    fits TMEM densely:
 //        S^T[128 tok, 64 rows]   = K_tile[128, 576] . Q[64, 576]^T   (K-major A, K-major B)
@@ -73,14 +75,24 @@ constexpr int kOffSlots = 0;
 constexpr int kOffQ = kOffSlots + kNumSlots * kSlotBytes;
 constexpr int kOffMisc = kOffQ + kNumChunks * kQChunkBytes;
 
+// One claimed work item as published by the producer to the other roles.
+struct WorkEntry {
+  int w;          // item index, -1 = no more work
+  int b, seg, q0, row_base, n_rows, seg_lo, seg_hi, n_tiles;
+  alignas(16) int lens[kRows];  // visible tokens of each of the block's rows (0 past n_rows)
+};
+constexpr int kWorkRing = 4;
+
 struct Misc {
   uint64_t full[kNumSlots];
   uint64_t ready[kNumSlots];  // fp8 only: slot expanded to bf16
   uint64_t empty[kNumSlots];
   uint64_t q_full, q_empty, s_full, p_full, o_done, fin;
+  uint64_t work_full[kWorkRing], work_empty[kWorkRing];
   uint32_t tmem_base;
   int abort;
-  alignas(16) int lens[kNumSoftmaxWarps][32];  // per-warp copy of its group's row lengths
+  WorkEntry work[kWorkRing];
+  int sm_stop[2];  // softmax warps' shared exit decision (double-buffered)
   float red[2][2][4][32];  // [buffer][column group][lane quarter][lane]
 };
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc)) + 1024;
@@ -96,6 +108,7 @@ struct Params {
   __nv_bfloat16 *out;
   float *lse;
   int *err;
+  int *sched;              // work-claim counter, zero at launch
   int64_t num_cache_rows;
   long long wait_budget;
   int subpage_stride;
@@ -121,46 +134,61 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// One work item, derived identically by every role from its index.
-struct Item {
-  int b, seg;
-  int q0;          // first verify row of the request
-  int row_base;    // flattened (t, h) index of column 0
-  int n_rows;      // query rows in this block (0: nothing to do at all)
-  int seg_lo, seg_hi, n_tiles;
-  bool bad_indptr, len_clipped;
-};
-
-__device__ __forceinline__ Item decode_item(const Params &p, int w) {
-  Item it{};
+// Decodes item w into a work entry (the whole producer warp): request, row
+// block, segment range, and the visible length of each row of the block.
+// Returns false when the request's qo_indptr is inconsistent (the item is
+// then published with no rows).  Requests with more than 32 verify rows read
+// the extra lengths directly.
+__device__ __forceinline__ bool decode_item(const Params &p, int w, WorkEntry &e, int lane,
+                                            bool &clipped) {
   const int S = p.num_segments;
-  it.seg = w % S;
+  const int seg = w % S;
   const int rb = (w / S) % p.row_blocks;
-  it.b = w / (S * p.row_blocks);
-  const int q0 = p.qo_indptr[it.b];
-  const int q1 = p.qo_indptr[it.b + 1];
-  it.q0 = q0;
-  if (q0 < 0 || q1 < q0 || q1 > p.num_rows || q1 - q0 > p.max_qlen) {
-    it.bad_indptr = true;
-    return it;
-  }
-  const int rows_req = (q1 - q0) * p.num_heads;
+  const int b = w / (S * p.row_blocks);
+  const int q0 = p.qo_indptr[b];
+  const int q1 = p.qo_indptr[b + 1];
+  clipped = false;
+  bool ok = !(q0 < 0 || q1 < q0 || q1 > p.num_rows || q1 - q0 > p.max_qlen);
+  const int qlen = ok ? q1 - q0 : 0;
+  const int rows_req = qlen * p.num_heads;
   const int row_begin = rb * kRows;
-  if (row_begin >= rows_req) return it;
-  it.n_rows = min(kRows, rows_req - row_begin);
-  it.row_base = q0 * p.num_heads + row_begin;
-  int group_len = 0;  // longest row of the request: fixes the segment partition
-  for (int t = q0; t < q1; ++t) {
-    int l = p.row_len[t];
-    if (l > p.max_len) { it.len_clipped = true; l = p.max_len; }
+  const int n_rows = row_begin < rows_req ? min(kRows, rows_req - row_begin) : 0;
+  // lengths of the request's rows: lane t holds row t (t < 32)
+  int my_len = 0;
+  if (lane < qlen) my_len = p.row_len[q0 + lane];
+  int group_len = 0;
+  for (int t = lane; t < qlen; t += 32) {
+    int l = t == lane ? my_len : p.row_len[q0 + t];
+    if (l > p.max_len) { clipped = true; l = p.max_len; }
     group_len = max(group_len, max(l, 0));
   }
-  const long long span = static_cast<long long>(S) * p.page_size;
-  const int seg_tokens = static_cast<int>((group_len + span - 1) / span) * p.page_size;
-  it.seg_lo = it.seg * seg_tokens;
-  it.seg_hi = min(it.seg_lo + seg_tokens, group_len);
-  it.n_tiles = it.seg_lo < it.seg_hi ? (it.seg_hi - it.seg_lo + kTileTok - 1) / kTileTok : 0;
-  return it;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) group_len = max(group_len, __shfl_xor_sync(0xffffffffu, group_len, o));
+  clipped = __any_sync(0xffffffffu, clipped);
+  // per-column lengths: column c is row (row_begin + c) / H of the request
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = lane + 32 * h;
+    const int t = (row_begin + c) / p.num_heads;
+    const int tt = t < 32 ? t : 0;
+    int l = __shfl_sync(0xffffffffu, my_len, tt);
+    if (t >= 32 && c < n_rows) l = p.row_len[q0 + t];
+    e.lens[c] = c < n_rows ? min(max(l, 0), p.max_len) : 0;
+  }
+  if (lane == 0) {
+    const long long span = static_cast<long long>(S) * p.page_size;
+    const int seg_tokens = static_cast<int>((group_len + span - 1) / span) * p.page_size;
+    e.w = w;
+    e.b = b;
+    e.seg = seg;
+    e.q0 = q0;
+    e.n_rows = n_rows;
+    e.row_base = q0 * p.num_heads + row_begin;
+    e.seg_lo = seg * seg_tokens;
+    e.seg_hi = min(e.seg_lo + seg_tokens, group_len);
+    e.n_tiles = (n_rows > 0 && e.seg_lo < e.seg_hi) ? (e.seg_hi - e.seg_lo + kTileTok - 1) / kTileTok : 0;
+  }
+  return ok;
 }
 
 // Warp transpose-reduce: on entry v[k] is this lane's value of column k; on
@@ -244,6 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&misc.p_full), kNumSoftmaxWarps);
     mbar_init(smem_u32(&misc.o_done), 1);
     mbar_init(smem_u32(&misc.fin), 1);
+    for (int i = 0; i < kWorkRing; ++i) {
+      mbar_init(smem_u32(&misc.work_full[i]), 1);
+      mbar_init(smem_u32(&misc.work_empty[i]), 1 + kNumSoftmaxWarps);
+    }
     misc.abort = 0;
     fence_mbar_init();
   }
@@ -260,37 +292,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == kProducerWarp) {
-    // ======================================================== TMA producer
+    // ======================================================== producer warp
+    // Claims work items (atomic counter), publishes them to the other roles
+    // through the work ring, and lane 0 issues the item's TMA loads.
+    const uint64_t pol_kv = l2_policy_evict_first();
+    const uint64_t pol_q = l2_policy_evict_last();
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_kv);
-      const uint64_t pol_kv = l2_policy_evict_first();
-      const uint64_t pol_q = l2_policy_evict_last();
-      const int page_bytes = P * (kFp8 ? 64 : 128);
-      // A slot is refilled only after its previous contents were consumed, so
-      // at most one load per slot is in flight: remember the latest one.
-      uint32_t armed = 0, armed_par = 0;
-      uint32_t g = 0, k = 0;  // running tile / item counters
-      bool ok = true;
-      for (int w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
-        const Item it = decode_item(p, w);
-        if (it.bad_indptr) {
-          record_error(p.err, MLA_DEV_BAD_INDPTR);
-          continue;
+    }
+    const int page_bytes = P * (kFp8 ? 64 : 128);
+    // A slot is refilled only after its previous contents were consumed, so
+    // at most one load per slot is in flight: remember the latest one.
+    uint32_t armed = 0, armed_par = 0;
+    uint32_t g = 0, kq = 0;  // running tile / Q-load counters
+    bool ok = true;
+    for (uint32_t k = 0;; ++k) {
+      const uint32_t ws = k % kWorkRing;
+      WorkEntry &e = misc.work[ws];
+      if (lane == 0 && ok &&
+          !mbar_wait(smem_u32(&misc.work_empty[ws]), ((k / kWorkRing) & 1u) ^ 1u, abort_flag, budget)) {
+        fail();
+        ok = false;
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      int w = 0;
+      if (lane == 0) w = ok ? atomicAdd(p.sched, 1) : p.num_items;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w >= p.num_items) {
+        if (lane == 0) {
+          e.w = -1;
+          mbar_arrive(smem_u32(&misc.work_full[ws]));
         }
-        if (it.len_clipped) record_error(p.err, MLA_DEV_LEN_BOUND);
-        if (it.n_rows == 0 || it.n_tiles == 0) continue;
+        break;
+      }
+      bool clipped = false;
+      const bool good = decode_item(p, w, e, lane, clipped);
+      __syncwarp();
+      if (lane == 0) {
+        if (!good) {
+          record_error(p.err, MLA_DEV_BAD_INDPTR);
+          e.n_rows = 0;
+          e.n_tiles = 0;
+        }
+        if (clipped) record_error(p.err, MLA_DEV_LEN_BOUND);
+        mbar_arrive(smem_u32(&misc.work_full[ws]));
+      }
+      const int n_tiles = __shfl_sync(0xffffffffu, lane == 0 ? e.n_tiles : 0, 0);
+      if (lane == 0 && n_tiles > 0) {
         // Q of this item, once the previous item's last QK is done with the buffer
-        if (!mbar_wait(smem_u32(&misc.q_empty), (k & 1u) ^ 1u, abort_flag, budget)) { fail(); ok = false; break; }
-        const uint32_t q_bar = smem_u32(&misc.q_full);
-        mbar_arrive_expect_tx(q_bar, kNumChunks * kQChunkBytes);
-        for (int c = 0; c < kNumChunks; ++c)
-          tma_load_2d(s_q + c * kQChunkBytes, &tm_q, q_bar, c * 64, it.row_base, pol_q);
-        ++k;
-        const int32_t *sp_row = p.subpage_table + static_cast<int64_t>(it.b) * p.subpage_stride;
-        for (int i = 0; i < it.n_tiles && ok; ++i, ++g) {
-          const int tok0 = it.seg_lo + i * kTileTok;
-          const int n_valid = min(kTileTok, it.seg_hi - tok0);
+        if (!mbar_wait(smem_u32(&misc.q_empty), (kq & 1u) ^ 1u, abort_flag, budget)) { fail(); ok = false; }
+        if (ok) {
+          const uint32_t q_bar = smem_u32(&misc.q_full);
+          mbar_arrive_expect_tx(q_bar, kNumChunks * kQChunkBytes);
+          for (int c = 0; c < kNumChunks; ++c)
+            tma_load_2d(s_q + c * kQChunkBytes, &tm_q, q_bar, c * 64, e.row_base, pol_q);
+        }
+        ++kq;
+        const int32_t *sp_row = p.subpage_table + static_cast<int64_t>(e.b) * p.subpage_stride;
+        for (int i = 0; i < n_tiles && ok; ++i, ++g) {
+          const int tok0 = e.seg_lo + i * kTileTok;
+          const int n_valid = min(kTileTok, e.seg_hi - tok0);
           const int n_pages = (n_valid + P - 1) / P;
           int32_t rows_of_page[kTileTok / 8];
 #pragma unroll
@@ -322,28 +384,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok || *abort_flag) {
-        // Let the copies already issued land before the CTA's memory is released.
-        const volatile int never = 0;
-        for (int c = 0; c < kNumSlots; ++c)
-          if (armed & (1u << c)) mbar_wait(smem_u32(&misc.full[c]), (armed_par >> c) & 1u, &never, budget);
-      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0 && (!ok || *abort_flag)) {
+      // Let the copies already issued land before the CTA's memory is released.
+      const volatile int never = 0;
+      for (int c = 0; c < kNumSlots; ++c)
+        if (armed & (1u << c)) mbar_wait(smem_u32(&misc.full[c]), (armed_par >> c) & 1u, &never, budget);
     }
   } else if (warp == kMmaWarp) {
     // ======================================================== UMMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kRows, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kRows, 1, 1);
-      uint32_t g = 0, k = 0;
+      uint32_t g = 0, kq = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
-        const Item it = decode_item(p, w);
-        if (it.bad_indptr || it.n_rows == 0 || it.n_tiles == 0) continue;
-        if (!mbar_wait(smem_u32(&misc.q_full), k & 1u, abort_flag, budget)) { fail(); break; }
-        ++k;
+      for (uint32_t k = 0; ok; ++k) {
+        const uint32_t ws = k % kWorkRing;
+        if (!mbar_wait(smem_u32(&misc.work_full[ws]), (k / kWorkRing) & 1u, abort_flag, budget)) { fail(); break; }
+        const WorkEntry &e = misc.work[ws];
+        const int w = e.w;
+        const int n_tiles = e.n_tiles, seg_lo = e.seg_lo, seg_hi = e.seg_hi;
+        if (w >= 0) mbar_arrive(smem_u32(&misc.work_empty[ws]));
+        if (w < 0) break;
+        if (n_tiles == 0) continue;
+        if (!mbar_wait(smem_u32(&misc.q_full), kq & 1u, abort_flag, budget)) { fail(); break; }
+        ++kq;
         tc_fence_after();
-        for (int i = 0; i < it.n_tiles; ++i, ++g) {
-          const int n_valid = min(kTileTok, it.seg_hi - (it.seg_lo + i * kTileTok));
+        for (int i = 0; i < n_tiles; ++i, ++g) {
+          const int n_valid = min(kTileTok, seg_hi - (seg_lo + i * kTileTok));
           const uint32_t par = g & 1u;
           for (int c = 0; c < kNumChunks; ++c) {
             const uint32_t bar = smem_u32(kFp8 ? &misc.ready[c] : &misc.full[c]);
@@ -357,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            sdesc_sw128(b0 + kk * 32, 0, 1024), idesc_qk, (c > 0 || kk > 0) ? 1u : 0u);
           }
           if (!ok) break;
-          if (i == it.n_tiles - 1) umma_commit(smem_u32(&misc.q_empty));  // Q free for the next item
+          if (i == n_tiles - 1) umma_commit(smem_u32(&misc.q_empty));  // Q free for the next item
           umma_commit(smem_u32(&misc.s_full));
           if (!mbar_wait(smem_u32(&misc.p_full), par, abort_flag, budget)) { fail(); ok = false; break; }
           tc_fence_after();
@@ -365,10 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int blk = 0; blk < 4; ++blk) {
             const uint32_t a0 = s_slots + (2 * blk) * kSlotBytes;
-            for (int kq = 0; kq < n_k16; ++kq)
-              umma_bf16_ss(tmem + kTmemO + blk * kRows, sdesc_sw128(a0 + kq * 2048, kSlotBytes, 1024),
-                           sdesc_sw128(s_p + kq * 2048, kSlotBytes, 1024), idesc_pv,
-                           (i > 0 || kq > 0) ? 1u : 0u);
+            for (int kk = 0; kk < n_k16; ++kk)
+              umma_bf16_ss(tmem + kTmemO + blk * kRows, sdesc_sw128(a0 + kk * 2048, kSlotBytes, 1024),
+                           sdesc_sw128(s_p + kk * 2048, kSlotBytes, 1024), idesc_pv,
+                           (i > 0 || kk > 0) ? 1u : 0u);
             umma_commit(smem_u32(&misc.empty[2 * blk]));
             umma_commit(smem_u32(&misc.empty[2 * blk + 1]));
           }
@@ -391,40 +460,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t g = 0;
 
-    for (int w = blockIdx.x; w < p.num_items; w += gridDim.x) {
-      const Item it = decode_item(p, w);
-      if (it.bad_indptr || it.n_rows == 0) continue;
-      if (it.n_tiles == 0) {
+    for (uint32_t k = 0;; ++k) {
+      const uint32_t ws = k % kWorkRing;
+      if (ok && !mbar_wait(smem_u32(&misc.work_full[ws]), (k / kWorkRing) & 1u, abort_flag, budget)) {
+        fail();
+        ok = false;
+      }
+      // All softmax warps take the same exit decision (they share named
+      // barriers below): one thread snapshots it between two barriers.
+      named_bar_sync(4, kNumSoftmaxWarps * 32);
+      if (threadIdx.x == 0) misc.sm_stop[k & 1u] = (*abort_flag != 0) || (misc.work[ws].w < 0);
+      named_bar_sync(4, kNumSoftmaxWarps * 32);
+      if (misc.sm_stop[k & 1u]) break;
+      const WorkEntry &e = misc.work[ws];
+      const int n_rows = e.n_rows, n_tiles = e.n_tiles, seg = e.seg;
+      const int row_base = e.row_base, seg_lo = e.seg_lo, seg_hi = e.seg_hi;
+      if (n_rows > 0 && n_tiles == 0) {
         // nothing visible in this segment for any row of the block
-        if (wq == 0 && my_col < it.n_rows) {
-          const int64_t r = it.row_base + my_col;
+        if (wq == 0 && my_col < n_rows) {
+          const int64_t r = row_base + my_col;
           if (direct) p.lse[r] = -INFINITY;
-          else { p.segm_max[r * S + it.seg] = -INFINITY; p.segm_sum[r * S + it.seg] = 0.0f; }
+          else { p.segm_max[r * S + seg] = -INFINITY; p.segm_sum[r * S + seg] = 0.0f; }
         }
-        if (direct && my_col < it.n_rows) {
-          uint4 *dst = reinterpret_cast<uint4 *>(p.out + (it.row_base + my_col) * 512);
-          for (int e = wq; e < 64; e += 4) dst[e] = make_uint4(0, 0, 0, 0);
+        if (direct && my_col < n_rows) {
+          uint4 *dst = reinterpret_cast<uint4 *>(p.out + (row_base + my_col) * 512);
+          for (int ee = wq; ee < 64; ee += 4) dst[ee] = make_uint4(0, 0, 0, 0);
         }
+      }
+      if (n_tiles == 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&misc.work_empty[ws]));
         continue;
       }
-      // this warp's copy of its 32 columns' visible lengths
-      {
-        int l = 0;
-        if (my_col < it.n_rows) {
-          const int t = (it.row_base - it.q0 * H + my_col) / H;
-          l = min(max(p.row_len[it.q0 + t], 0), p.max_len);
-        }
-        misc.lens[warp][lane] = l;
-        __syncwarp();
-      }
+      const int *lens_g = &e.lens[32 * g_col];
       float l_part[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) l_part[j] = 0.0f;
       float m_ref = -INFINITY;
 
-      for (int i = 0; i < it.n_tiles; ++i, ++g) {
-        const int tok0 = it.seg_lo + i * kTileTok;
-        const int n_valid = min(kTileTok, it.seg_hi - tok0);
+      for (int i = 0; i < n_tiles; ++i, ++g) {
+        const int tok0 = seg_lo + i * kTileTok;
+        const int n_valid = min(kTileTok, seg_hi - tok0);
         const uint32_t par = g & 1u;
 
         if constexpr (kFp8) {
@@ -469,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool tok_in = tok < n_valid;
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          const int4 lens = *reinterpret_cast<const int4 *>(&misc.lens[warp][4 * j4]);
+          const int4 lens = *reinterpret_cast<const int4 *>(&lens_g[4 * j4]);
           const int lv[4] = {lens.x, lens.y, lens.z, lens.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -561,37 +637,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float l_tot = misc.red[red_buf][g_col][0][lane] + misc.red[red_buf][g_col][1][lane] +
                           misc.red[red_buf][g_col][2][lane] + misc.red[red_buf][g_col][3][lane];
       red_buf ^= 1;
-      ok = ok && (*abort_flag == 0);
-      if (ok && wq == 0 && my_col < it.n_rows) {
-        const int64_t r = it.row_base + my_col;
+      const bool write = ok && (*abort_flag == 0);
+      if (write && wq == 0 && my_col < n_rows) {
+        const int64_t r = row_base + my_col;
         if (direct) {
           p.lse[r] = (l_tot > 0.0f) ? (m_ref + __log2f(l_tot)) * kLn2 : -INFINITY;
         } else {
-          p.segm_max[r * S + it.seg] = (l_tot > 0.0f) ? m_ref : -INFINITY;
-          p.segm_sum[r * S + it.seg] = l_tot;
+          p.segm_max[r * S + seg] = (l_tot > 0.0f) ? m_ref : -INFINITY;
+          p.segm_sum[r * S + seg] = l_tot;
         }
       }
       const float col_scale = (l_tot > 0.0f) ? (direct ? p.out_scale / l_tot : p.out_scale) : 0.0f;
-      const int n_cols = min(32, it.n_rows - 32 * g_col);
+      const int n_cols = min(32, n_rows - 32 * g_col);
 #pragma unroll 1
       for (int blk = 0; blk < 4; ++blk) {
         uint32_t ov[32];
         tmem_ld32(tmem + lane_addr + kTmemO + blk * kRows + 32 * g_col, ov);
-        if (!ok) continue;
+        if (!write) continue;
         const int dim = blk * 128 + tok;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float sc = __shfl_sync(0xffffffffu, col_scale, j);
           const float lj = __shfl_sync(0xffffffffu, l_tot, j);
           if (j < n_cols) {
-            const int64_t r = it.row_base + 32 * g_col + j;
+            const int64_t r = row_base + 32 * g_col + j;
             const float v = __uint_as_float(ov[j]) * sc;
             if (direct) p.out[r * 512 + dim] = __float2bfloat16_rn(v);
-            else if (lj > 0.0f) p.segm_out[(r * S + it.seg) * 512 + dim] = v;
+            else if (lj > 0.0f) p.segm_out[(r * S + seg) * 512 + dim] = v;
           }
         }
       }
       tc_fence_before();  // O reads done before the next item's first PV overwrites O
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&misc.work_empty[ws]));
     }
   }
 
@@ -656,6 +734,7 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.lse = a.lse;
   p.err = d.err;
+  p.sched = d.sched;
   p.num_cache_rows = a.num_cache_rows;
   p.wait_budget = 4000000000LL;  // ~2 s of SM clock
   p.subpage_stride = a.subpage_stride;
@@ -677,6 +756,8 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
   p.out_scale = kv_scale;
 
   const int grid = static_cast<int>(items < g_num_sms[dev] ? items : g_num_sms[dev]);
+  e = cudaMemsetAsync(d.sched, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(work counter)");
   kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");

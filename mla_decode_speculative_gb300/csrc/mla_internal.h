@@ -25,24 +25,34 @@ mla_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType 
                         uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 // Launchers (arguments already validated on the host).
+struct TableLaunch {  // optional sub-page expansion (block_table == nullptr: none)
+  const int32_t *block_table;
+  int bt_stride, num_blocks, block_size, page_size;
+  int32_t *subpage_table;
+  int sp_stride;
+};
 mla_status launch_plan_rows(int num_reqs, int num_rows, const int32_t *seq_lens,
                             const int32_t *qo_indptr, int32_t *row_len, int32_t *row_req,
-                            int *err, cudaStream_t stream);
+                            const TableLaunch &table, int *err, cudaStream_t stream);
 mla_status launch_shard_rows(int num_reqs, int num_rows, const int32_t *qo_indptr,
                              const int32_t *row_len_global, int world_size, int rank,
-                             int32_t *row_len_local, int *err, cudaStream_t stream);
-mla_status launch_subpage_table(int num_reqs, const int32_t *qo_indptr, const int32_t *row_len,
-                                const int32_t *block_table, int bt_stride, int num_blocks,
-                                int block_size, int page_size, int32_t *subpage_table,
-                                int sp_stride, int *err, cudaStream_t stream);
+                             int32_t *row_len_local, const TableLaunch &table, int *err,
+                             cudaStream_t stream);
 
 struct DecodeLaunch {
   const mla_decode_args *a;
   float *segm_out;
   float *segm_max;
   float *segm_sum;
+  int *sched;  // work-claim counter (workspace), zeroed before each launch
   int *err;
 };
+// Workspace layout of mla_decode_verify: [segm_out][segm_max][segm_sum] (only
+// when num_segments > 1, 256-byte aligned regions) then the work counter.
+struct WorkspaceLayout {
+  size_t segm_out, segm_max, segm_sum, sched, total;
+};
+WorkspaceLayout decode_workspace_layout(const mla_decode_args &a);
 mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream);
 
 struct MergeLaunch {
@@ -60,6 +70,8 @@ struct MergeLaunch {
   const int32_t *live_rows;  // optional device int: rows (t) actually present; nullptr = all
 };
 mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream);
+
+constexpr int kMaxParts = 1024;  // most split-K segments / shards one merge combines
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 

@@ -13,9 +13,9 @@
 // An empty part (max / lse = -inf) is never read; all parts empty gives
 // out = 0, lse = -inf.
 //
-// HBM-bound streaming reduction: one warp per (row, head); each lane owns 16
-// of the 512 output dims, reads each live part with 16-byte streaming loads
-// (4 parts in flight per lane) and writes 32 contiguous bytes of bf16.
+// HBM-bound streaming reduction: one 128-thread block per (row, head); each
+// thread owns 4 of the 512 output dims, reads each live part with one
+// streaming load (8 parts in flight per thread) and writes 8 bytes of bf16.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -27,7 +27,7 @@
 namespace mla {
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
+constexpr int kThreadsPerItem = 128;  // 512 dims / 4 per thread
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct MergeParams {
@@ -58,44 +58,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
 }
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float *f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    f[2 * k] = __uint_as_float(w[k] << 16);
-    f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-  }
-}
-
-// Loads this lane's 16 dims of part `s` of item `it`.
+// One 128-thread block per (row, head): thread t owns output dims 4t..4t+3,
+// so every live part costs each thread one 16-byte (f32) or 8-byte (bf16)
+// load, and up to 8 parts are in flight per thread.
 template <bool kSeg>
-__device__ __forceinline__ void load_part(const MergeParams &p, int64_t it, int s, int lane, float *v) {
-  if constexpr (kSeg) {
-    const float4 *src = reinterpret_cast<const float4 *>(
-        p.segm_out + (it * p.num_parts + s) * 512 + lane * 16);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 x = __ldcs(src + k);
-      v[4 * k + 0] = x.x;
-      v[4 * k + 1] = x.y;
-      v[4 * k + 2] = x.z;
-      v[4 * k + 3] = x.w;
-    }
-  } else {
-    const uint4 *src = reinterpret_cast<const uint4 *>(
-        p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512 + lane * 16);
-    const uint4 a = __ldcs(src);
-    const uint4 b = __ldcs(src + 1);
-    bf16x8_to_f32(a, v);
-    bf16x8_to_f32(b, v + 8);
-  }
-}
-
-template <bool kSeg>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t it = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (it >= p.num_items) return;
+__global__ void __launch_bounds__(kThreadsPerItem) merge_kernel(const MergeParams p) {
+  __shared__ float s_w[kMaxParts];
+  __shared__ int s_idx[kMaxParts];
+  __shared__ float s_red[kThreadsPerItem / 32];
+  __shared__ int s_cnt[kThreadsPerItem / 32];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int64_t it = blockIdx.x;
   if (p.live_rows != nullptr && it / p.num_heads >= static_cast<int64_t>(*p.live_rows)) return;
   const int n = p.num_parts;
 
@@ -104,67 +78,91 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
     if constexpr (kSeg) return p.segm_max[it * n + s];
     else return p.part_lse[static_cast<int64_t>(s) * p.num_items + it];
   };
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, stat(s));
-  M = warp_max(M);
-
-  float acc[16];
+  float m_loc = -INFINITY;
+  for (int s = tid; s < n; s += kThreadsPerItem) m_loc = fmaxf(m_loc, stat(s));
+  m_loc = warp_max(m_loc);
+  if (lane == 0) s_red[warp] = m_loc;
+  __syncthreads();
+  float M = s_red[0];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
-  uint4 *dst = reinterpret_cast<uint4 *>(p.out + it * 512 + lane * 16);
+  for (int k = 1; k < kThreadsPerItem / 32; ++k) M = fmaxf(M, s_red[k]);
+  __syncthreads();
+
+  uint2 *dst = reinterpret_cast<uint2 *>(p.out + it * 512) + tid;
   if (M == -INFINITY) {
-    dst[0] = make_uint4(0, 0, 0, 0);
-    dst[1] = make_uint4(0, 0, 0, 0);
-    if (lane == 0) p.lse[it] = -INFINITY;
+    *dst = make_uint2(0, 0);
+    if (tid == 0) p.lse[it] = -INFINITY;
     return;
   }
-
-  // denominator
-  float den = 0.0f;
-  for (int s = lane; s < n; s += 32) {
-    const float m = stat(s);
-    if (m != -INFINITY) {
-      if constexpr (kSeg) den += exp2f(m - M) * p.segm_sum[it * n + s];
-      else den += expf(m - M);
-    }
-  }
-  den = warp_sum(den);
-  const float inv_den = 1.0f / den;
-
-  // weighted sum, parts in chunks of 32 (lane s%32 holds part s's weight)
-  for (int base = 0; base < n; base += 32) {
+  // unnormalised weights and the denominator; live parts are compacted, in
+  // order, into (s_idx, s_w) so the load loop below has no conditionals
+  float d_loc = 0.0f;
+  int n_live = 0;
+  for (int base = 0; base < n; base += kThreadsPerItem) {
+    const int s = base + tid;
     float wgt = 0.0f;
-    if (base + lane < n) {
-      const float m = stat(base + lane);
-      if (m != -INFINITY) wgt = (kSeg ? exp2f(m - M) : expf(m - M)) * inv_den;
-    }
-    const int cnt = min(32, n - base);
-    for (int s0 = 0; s0 < cnt; s0 += 4) {
-      float v[4][16];
-      float w4[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int sl = s0 + u;
-        w4[u] = __shfl_sync(0xffffffffu, wgt, sl & 31);
-        if (sl < cnt && w4[u] != 0.0f) {
-          load_part<kSeg>(p, it, base + sl, lane, v[u]);
+    if (s < n) {
+      const float m = stat(s);
+      if (m != -INFINITY) {
+        if constexpr (kSeg) {
+          wgt = exp2f(m - M);
+          d_loc += wgt * p.segm_sum[it * n + s];
         } else {
-          w4[u] = 0.0f;
-#pragma unroll
-          for (int k = 0; k < 16; ++k) v[u][k] = 0.0f;
+          wgt = expf(m - M);
+          d_loc += wgt;
         }
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k] = fmaf(w4[u], v[u][k], acc[k]);
     }
+    const unsigned live = __ballot_sync(0xffffffffu, wgt != 0.0f);
+    if (lane == 0) s_cnt[warp] = __popc(live);
+    __syncthreads();
+    int off = n_live;
+    for (int k = 0; k < warp; ++k) off += s_cnt[k];
+    if (wgt != 0.0f) {
+      const int pos = off + __popc(live & ((1u << lane) - 1u));
+      s_w[pos] = wgt;
+      s_idx[pos] = s;
+    }
+    for (int k = 0; k < kThreadsPerItem / 32; ++k) n_live += s_cnt[k];
+    __syncthreads();
   }
-  dst[0] = make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
-                      pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
-  dst[1] = make_uint4(pack_bf16(acc[8], acc[9]), pack_bf16(acc[10], acc[11]),
-                      pack_bf16(acc[12], acc[13]), pack_bf16(acc[14], acc[15]));
-  if (lane == 0) p.lse[it] = kSeg ? (M + log2f(den)) * kLn2 : M + logf(den);
+  d_loc = warp_sum(d_loc);
+  if (lane == 0) s_red[warp] = d_loc;
+  __syncthreads();
+  float den = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kThreadsPerItem / 32; ++k) den += s_red[k];
+  const float inv_den = 1.0f / den;
+
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int k0 = 0; k0 < n_live; k0 += 8) {
+    float v[8][4];
+    float wv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = min(k0 + u, n_live - 1);  // padding re-reads the last live part, weight 0
+      const int s = s_idx[k];
+      wv[u] = (k0 + u < n_live) ? s_w[k] : 0.0f;
+      if constexpr (kSeg) {
+        const float4 x = __ldcs(reinterpret_cast<const float4 *>(p.segm_out + (it * n + s) * 512) + tid);
+        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+      } else {
+        const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(
+                                   p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512) + tid);
+        v[u][0] = __uint_as_float(x.x << 16);
+        v[u][1] = __uint_as_float(x.x & 0xffff0000u);
+        v[u][2] = __uint_as_float(x.y << 16);
+        v[u][3] = __uint_as_float(x.y & 0xffff0000u);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c] = fmaf(wv[u], v[u][c], acc[c]);
+  }
+  *dst = make_uint2(pack_bf16(acc[0] * inv_den, acc[1] * inv_den),
+                    pack_bf16(acc[2] * inv_den, acc[3] * inv_den));
+  if (tid == 0) p.lse[it] = kSeg ? (M + log2f(den)) * kLn2 : M + logf(den);
 }
 
 }  // namespace
@@ -183,11 +181,15 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
   p.num_heads = m.num_heads;
   p.num_parts = m.num_parts;
   if (p.num_items == 0) return MLA_OK;
-  const int64_t blocks = (p.num_items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  if (p.num_items > INT32_MAX) {
+    set_error("mla_merge_segments: too many (row, head) items");
+    return MLA_ERR_UNSUPPORTED;
+  }
+  const unsigned blocks = static_cast<unsigned>(p.num_items);
   if (m.mode == MLA_MERGE_SEGMENTS)
-    merge_kernel<true><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(p);
+    merge_kernel<true><<<blocks, kThreadsPerItem, 0, stream>>>(p);
   else
-    merge_kernel<false><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(p);
+    merge_kernel<false><<<blocks, kThreadsPerItem, 0, stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return MLA_OK;

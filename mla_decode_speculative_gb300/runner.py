@@ -45,11 +45,11 @@ class VerifyStep:
                                         dtype=torch.bfloat16, device=dev)
             self.part_lse = torch.empty((world_size, num_rows, num_heads), dtype=torch.float32,
                                         device=dev)
-        ws = 0
+        ws = 256  # scheduler state
         if num_segments > 1:
             items = num_rows * num_heads * num_segments
-            ws = ((items * 512 * 4 + 255) & ~255) + 2 * ((items * 4 + 255) & ~255)
-        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+            ws += ((items * 512 * 4 + 255) & ~255) + 2 * ((items * 4 + 255) & ~255)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
 
     def __call__(self, q: torch.Tensor, kv_cache: torch.Tensor, seq_lens: torch.Tensor,
                  qo_indptr: torch.Tensor, block_tables: torch.Tensor, sm_scale: float,
