@@ -238,6 +238,28 @@ typedef struct mla_merge_args {
  * All parts empty: out = 0, lse = -inf.  out is rounded to bf16 (RNE). */
 mla_status mla_merge_segments(const mla_merge_args *a, mla_stream_t stream);
 
+/* Owner-filtered paged write of the new verify tokens -- the step right before
+ * the decode [sglang #34432, 实现拆解 4 and forward_mla_rocm.py snippet:
+ * set_mla_kv_buffer filters by owner and divides by the shard count; key
+ * snippet g(j) = j * W + r].  Request b's qlen_b new tokens (rows
+ * qo_indptr[b] .. qo_indptr[b+1]-1 of kv_new, each [576] bf16 = k_nope then
+ * k_pe) sit at global positions g = L_b - qlen_b + t.  Rank `rank` of
+ * `world_size` keeps the tokens with g mod W == rank, at its local index
+ * j = g div W: cache row block_table[b][j / block_size] * block_size +
+ * j % block_size of this rank's cache [num_cache_rows, 576].  world_size = 1
+ * is the plain (unsharded) write.  bf16 caches receive the values unchanged;
+ * fp8 caches (kv_dtype = MLA_KV_FP8_E4M3) receive the e4m3 codes of
+ * value / kv_scale computed in float32, rounded to nearest even and
+ * saturated to +-448.  Only interleave 1 is supported.
+ * Device checks: MLA_DEV_BAD_INDPTR, MLA_DEV_BAD_QLEN, MLA_DEV_BAD_BLOCK_ID
+ * (the token is then not written). */
+mla_status mla_write_kv(int num_reqs, int num_rows, const int32_t *seq_lens,
+                        const int32_t *qo_indptr, const void *kv_new, int world_size,
+                        int rank, int interleave, const int32_t *block_table,
+                        int block_table_stride, int num_blocks, int block_size,
+                        void *kv_cache, int kv_dtype, float kv_scale,
+                        int64_t num_cache_rows, mla_stream_t stream);
+
 /* The same decode / verify as mla_decode_verify, for callers that cannot
  * allocate device memory where they make the call -- code running under
  * CUDA-graph capture (cudaMalloc is not allowed there), serving runtimes that

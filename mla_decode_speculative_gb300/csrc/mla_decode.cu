@@ -250,7 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int H = p.num_heads;
   const int S = p.num_segments;
   const int P = p.page_size;
   const bool direct = (S == 1);
@@ -301,6 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_kv);
     }
+    // (Lane 0 waits and posts the expected bytes; every lane issues the TMA
+    // copies of the sub-page it owns.)
     const int page_bytes = P * (kFp8 ? 64 : 128);
     // A slot is refilled only after its previous contents were consumed, so
     // at most one load per slot is in flight: remember the latest one.
@@ -339,46 +340,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(smem_u32(&misc.work_full[ws]));
       }
       const int n_tiles = __shfl_sync(0xffffffffu, lane == 0 ? e.n_tiles : 0, 0);
-      if (lane == 0 && n_tiles > 0) {
+      if (n_tiles > 0) {
+        const int seg_lo = e.seg_lo, seg_hi = e.seg_hi, row_base = e.row_base;
         // Q of this item, once the previous item's last QK is done with the buffer
-        if (!mbar_wait(smem_u32(&misc.q_empty), (kq & 1u) ^ 1u, abort_flag, budget)) { fail(); ok = false; }
+        if (lane == 0 && ok &&
+            !mbar_wait(smem_u32(&misc.q_empty), (kq & 1u) ^ 1u, abort_flag, budget)) {
+          fail();
+          ok = false;
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        const uint32_t q_bar = smem_u32(&misc.q_full);
         if (ok) {
-          const uint32_t q_bar = smem_u32(&misc.q_full);
-          mbar_arrive_expect_tx(q_bar, kNumChunks * kQChunkBytes);
-          for (int c = 0; c < kNumChunks; ++c)
-            tma_load_2d(s_q + c * kQChunkBytes, &tm_q, q_bar, c * 64, e.row_base, pol_q);
+          if (lane == 0) mbar_arrive_expect_tx(q_bar, kNumChunks * kQChunkBytes);
+          __syncwarp();
+          if (lane < kNumChunks)
+            tma_load_2d(s_q + lane * kQChunkBytes, &tm_q, q_bar, lane * 64, row_base, pol_q);
         }
         ++kq;
         const int32_t *sp_row = p.subpage_table + static_cast<int64_t>(e.b) * p.subpage_stride;
         for (int i = 0; i < n_tiles && ok; ++i, ++g) {
-          const int tok0 = e.seg_lo + i * kTileTok;
-          const int n_valid = min(kTileTok, e.seg_hi - tok0);
+          const int tok0 = seg_lo + i * kTileTok;
+          const int n_valid = min(kTileTok, seg_hi - tok0);
           const int n_pages = (n_valid + P - 1) / P;
-          int32_t rows_of_page[kTileTok / 8];
-#pragma unroll
-          for (int j = 0; j < kTileTok / 8; ++j) {
-            int32_t r = 0;
-            if (j < n_pages) {
-              const int32_t id = sp_row[tok0 / P + j];
-              if (id < 0 || static_cast<int64_t>(id) * P + P > p.num_cache_rows) {
-                record_error(p.err, MLA_DEV_BAD_SUBPAGE);
-                r = static_cast<int32_t>(p.num_cache_rows);  // out of range: zero fill
-              } else {
-                r = id * P;
-              }
+          // lane j owns sub-page j of the tile: one id fetch per tile, held in a register
+          int32_t my_row = 0;
+          if (lane < n_pages) {
+            const int32_t id = sp_row[tok0 / P + lane];
+            if (id < 0 || static_cast<int64_t>(id) * P + P > p.num_cache_rows) {
+              record_error(p.err, MLA_DEV_BAD_SUBPAGE);
+              my_row = static_cast<int32_t>(p.num_cache_rows);  // out of range: zero fill
+            } else {
+              my_row = id * P;
             }
-            rows_of_page[j] = r;
           }
           const uint32_t wpar = (g & 1u) ^ 1u;
           for (int c = 0; c < kNumChunks; ++c) {
-            if (!mbar_wait(smem_u32(&misc.empty[c]), wpar, abort_flag, budget)) { fail(); ok = false; break; }
+            if (lane == 0 && !mbar_wait(smem_u32(&misc.empty[c]), wpar, abort_flag, budget)) {
+              fail();
+              ok = false;
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
             const uint32_t fbar = smem_u32(&misc.full[c]);
-            mbar_arrive_expect_tx(fbar, n_pages * page_bytes);
+            if (lane == 0) mbar_arrive_expect_tx(fbar, n_pages * page_bytes);
+            __syncwarp();  // the expected bytes are posted before any copy can complete
             const uint32_t dst = s_slots + c * kSlotBytes + (kFp8 ? kSlotBytes / 2 : 0);
-#pragma unroll
-            for (int j = 0; j < kTileTok / 8; ++j)
-              if (j < n_pages)
-                tma_load_2d(dst + j * page_bytes, &tm_kv, fbar, c * 64, rows_of_page[j], pol_kv);
+            if (lane < n_pages)
+              tma_load_2d(dst + lane * page_bytes, &tm_kv, fbar, c * 64, my_row, pol_kv);
             armed |= 1u << c;
             armed_par = (armed_par & ~(1u << c)) | ((g & 1u) << c);
           }
@@ -494,8 +502,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int *lens_g = &e.lens[32 * g_col];
       float l_part[32];
+      float m_col[32];  // reference max of each of the group's columns (lane j keeps m_ref of column j)
 #pragma unroll
-      for (int j = 0; j < 32; ++j) l_part[j] = 0.0f;
+      for (int j = 0; j < 32; ++j) {
+        l_part[j] = 0.0f;
+        m_col[j] = -INFINITY;
+      }
       float m_ref = -INFINITY;
 
       for (int i = 0; i < n_tiles; ++i, ++g) {
@@ -553,28 +565,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             x[j] = (tok_in && gtok < lv[u]) ? __uint_as_float(sv[j]) * p.score_scale_log2 : -INFINITY;
           }
         }
-        // column max over the 128 tokens of the tile
-        float red[32];
+        // The column max is needed only when some score exceeds the column's
+        // reference by more than the lazy-rescale threshold (always on the
+        // first tile that sees data).  One barrier-reduction votes per group.
+        bool exceed = false;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) red[j] = x[j];
-        const float wmax = warp_reduce_scatter<true>(red, lane);
-        misc.red[red_buf][g_col][wq][lane] = wmax;
-        named_bar_sync(1 + g_col, 128);
-        const float tmax = fmaxf(fmaxf(misc.red[red_buf][g_col][0][lane], misc.red[red_buf][g_col][1][lane]),
-                                 fmaxf(misc.red[red_buf][g_col][2][lane], misc.red[red_buf][g_col][3][lane]));
-        red_buf ^= 1;
+        for (int j = 0; j < 32; ++j) exceed |= (x[j] - m_col[j] > kRescaleThreshold);
+        const bool group_exceed = named_bar_red_or(1 + g_col, 128, exceed);
+        bool any_rescale = false;
         float alpha = 1.0f;
-        if (tmax > m_ref + kRescaleThreshold) {
-          alpha = fast_exp2(m_ref - tmax);  // 0 when m_ref is -inf
-          m_ref = tmax;
-        }
-        const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-        const bool any_rescale = __any_sync(0xffffffffu, alpha != 1.0f);
+        if (group_exceed) {
+          float red[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float mj = __shfl_sync(0xffffffffu, m_use, j);
-          x[j] = fast_exp2(x[j] - mj);  // probability (0 for masked entries)
+          for (int j = 0; j < 32; ++j) red[j] = x[j];
+          const float wmax = warp_reduce_scatter<true>(red, lane);
+          misc.red[red_buf][g_col][wq][lane] = wmax;
+          named_bar_sync(1 + g_col, 128);
+          const float tmax =
+              fmaxf(fmaxf(misc.red[red_buf][g_col][0][lane], misc.red[red_buf][g_col][1][lane]),
+                    fmaxf(misc.red[red_buf][g_col][2][lane], misc.red[red_buf][g_col][3][lane]));
+          red_buf ^= 1;
+          if (tmax > m_ref + kRescaleThreshold) {
+            alpha = fast_exp2(m_ref - tmax);  // 0 when m_ref is -inf
+            m_ref = tmax;
+          }
+          any_rescale = __any_sync(0xffffffffu, alpha != 1.0f);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) m_col[j] = __shfl_sync(0xffffffffu, m_ref, j);
         }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)  // probability (0 for masked entries and empty columns)
+          x[j] = (x[j] == -INFINITY) ? 0.0f : fast_exp2(x[j] - m_col[j]);
         if (any_rescale) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) l_part[j] *= __shfl_sync(0xffffffffu, alpha, j);
@@ -649,22 +670,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float col_scale = (l_tot > 0.0f) ? (direct ? p.out_scale / l_tot : p.out_scale) : 0.0f;
       const int n_cols = min(32, n_rows - 32 * g_col);
+      // column j's scale (0: the row saw no token here) gathered once for all four blocks
+      float sc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sc[j] = __shfl_sync(0xffffffffu, col_scale, j);
+      const int64_t r0 = row_base + 32 * g_col;
 #pragma unroll 1
       for (int blk = 0; blk < 4; ++blk) {
         uint32_t ov[32];
         tmem_ld32(tmem + lane_addr + kTmemO + blk * kRows + 32 * g_col, ov);
         if (!write) continue;
         const int dim = blk * 128 + tok;
+        if (direct) {
+          __nv_bfloat16 *o = p.out + r0 * 512 + dim;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float sc = __shfl_sync(0xffffffffu, col_scale, j);
-          const float lj = __shfl_sync(0xffffffffu, l_tot, j);
-          if (j < n_cols) {
-            const int64_t r = row_base + 32 * g_col + j;
-            const float v = __uint_as_float(ov[j]) * sc;
-            if (direct) p.out[r * 512 + dim] = __float2bfloat16_rn(v);
-            else if (lj > 0.0f) p.segm_out[(r * S + seg) * 512 + dim] = v;
-          }
+          for (int j = 0; j < 32; ++j)
+            if (j < n_cols) o[static_cast<int64_t>(j) * 512] = __float2bfloat16_rn(__uint_as_float(ov[j]) * sc[j]);
+        } else {
+          float *o = p.segm_out + (r0 * S + seg) * 512 + dim;
+          const int64_t stride = static_cast<int64_t>(S) * 512;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < n_cols && sc[j] != 0.0f) o[j * stride] = __uint_as_float(ov[j]) * sc[j];
         }
       }
       tc_fence_before();  // O reads done before the next item's first PV overwrites O

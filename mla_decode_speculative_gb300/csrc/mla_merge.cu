@@ -58,6 +58,77 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
 }
+// Loads this thread's 4 dims of part s of item it.
+template <bool kSeg>
+__device__ __forceinline__ float4 load4(const MergeParams &p, int64_t it, int s, int tid) {
+  if constexpr (kSeg) {
+    return __ldcs(reinterpret_cast<const float4 *>(p.segm_out + (it * p.num_parts + s) * 512) + tid);
+  } else {
+    const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(
+                               p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512) + tid);
+    return make_float4(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u),
+                       __uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
+  }
+}
+
+// Up to 32 parts: no block barrier.  Every thread reads the item's (tiny,
+// L1-broadcast) statistics itself, so the loads of all live parts are issued
+// together, one dependent round trip after the statistics.
+template <bool kSeg>
+__global__ void __launch_bounds__(kThreadsPerItem) merge_kernel_small(const MergeParams p) {
+  const int tid = threadIdx.x;
+  const int64_t it = blockIdx.x;
+  if (p.live_rows != nullptr && it / p.num_heads >= static_cast<int64_t>(*p.live_rows)) return;
+  const int n = p.num_parts;
+  float m[32], l[32];
+#pragma unroll
+  for (int s = 0; s < 32; ++s) {
+    m[s] = -INFINITY;
+    l[s] = 0.0f;
+    if (s < n) {
+      if constexpr (kSeg) {
+        m[s] = p.segm_max[it * n + s];
+        l[s] = p.segm_sum[it * n + s];
+      } else {
+        m[s] = p.part_lse[static_cast<int64_t>(s) * p.num_items + it];
+      }
+    }
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < 32; ++s) M = fmaxf(M, m[s]);
+  uint2 *dst = reinterpret_cast<uint2 *>(p.out + it * 512) + tid;
+  if (M == -INFINITY) {
+    *dst = make_uint2(0, 0);
+    if (tid == 0) p.lse[it] = -INFINITY;
+    return;
+  }
+  float den = 0.0f;
+#pragma unroll
+  for (int s = 0; s < 32; ++s) {
+    float w = 0.0f;
+    if (m[s] != -INFINITY) w = kSeg ? exp2f(m[s] - M) : expf(m[s] - M);
+    den += kSeg ? w * l[s] : w;
+    m[s] = w;  // m now holds the weights
+  }
+  float4 v[32];
+#pragma unroll
+  for (int s = 0; s < 32; ++s)
+    v[s] = (m[s] != 0.0f) ? load4<kSeg>(p, it, s, tid) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int s = 0; s < 32; ++s) {
+    acc[0] = fmaf(m[s], v[s].x, acc[0]);
+    acc[1] = fmaf(m[s], v[s].y, acc[1]);
+    acc[2] = fmaf(m[s], v[s].z, acc[2]);
+    acc[3] = fmaf(m[s], v[s].w, acc[3]);
+  }
+  const float inv_den = 1.0f / den;
+  *dst = make_uint2(pack_bf16(acc[0] * inv_den, acc[1] * inv_den),
+                    pack_bf16(acc[2] * inv_den, acc[3] * inv_den));
+  if (tid == 0) p.lse[it] = kSeg ? (M + log2f(den)) * kLn2 : M + logf(den);
+}
+
 // One 128-thread block per (row, head): thread t owns output dims 4t..4t+3,
 // so every live part costs each thread one 16-byte (f32) or 8-byte (bf16)
 // load, and up to 8 parts are in flight per thread.
@@ -186,10 +257,14 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
     return MLA_ERR_UNSUPPORTED;
   }
   const unsigned blocks = static_cast<unsigned>(p.num_items);
-  if (m.mode == MLA_MERGE_SEGMENTS)
-    merge_kernel<true><<<blocks, kThreadsPerItem, 0, stream>>>(p);
-  else
-    merge_kernel<false><<<blocks, kThreadsPerItem, 0, stream>>>(p);
+  const bool small = p.num_parts <= 32;
+  if (m.mode == MLA_MERGE_SEGMENTS) {
+    if (small) merge_kernel_small<true><<<blocks, kThreadsPerItem, 0, stream>>>(p);
+    else merge_kernel<true><<<blocks, kThreadsPerItem, 0, stream>>>(p);
+  } else {
+    if (small) merge_kernel_small<false><<<blocks, kThreadsPerItem, 0, stream>>>(p);
+    else merge_kernel<false><<<blocks, kThreadsPerItem, 0, stream>>>(p);
+  }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return MLA_OK;

@@ -68,7 +68,7 @@ class MergeArgs(ctypes.Structure):
 _lib = None
 _lock = threading.Lock()
 EXPORTS = ("mla_page_size", "mla_plan_rows", "mla_shard_row_view", "mla_decode_verify_workspace",
-           "mla_decode_verify", "mla_decode_verify_noalloc", "mla_merge_segments", "mla_get_device_error",
+           "mla_decode_verify", "mla_decode_verify_noalloc", "mla_write_kv", "mla_merge_segments", "mla_get_device_error",
            "mla_last_error_string", "mla_status_string", "mla_abi_version")
 
 
@@ -102,6 +102,9 @@ def lib():
         L.mla_decode_verify.restype = c_int
         L.mla_decode_verify_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), vp]
         L.mla_decode_verify_noalloc.restype = c_int
+        L.mla_write_kv.argtypes = [c_int, c_int, i32p, i32p, vp, c_int, c_int, c_int, i32p, c_int,
+                                   c_int, c_int, vp, c_int, ctypes.c_float, ctypes.c_int64, vp]
+        L.mla_write_kv.restype = c_int
         L.mla_merge_segments.argtypes = [ctypes.POINTER(MergeArgs), vp]
         L.mla_merge_segments.restype = c_int
         L.mla_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
@@ -320,6 +323,23 @@ def merge_states(part_out, part_lse, out=None, lse=None, stream=None):
     m.lse = _ptr(lse, torch.float32, "lse")
     _check(lib().mla_merge_segments(ctypes.byref(m), _stream(stream)), "mla_merge_segments")
     return out, lse
+
+
+def write_kv(seq_lens, qo_indptr, kv_new, kv_cache, block_table, num_blocks, block_size,
+             world_size=1, rank=0, kv_scale=1.0, interleave=1, stream=None):
+    """mla_write_kv: owner-filtered paged write of the new tokens (kv_new [T, 576]
+    bf16) into this rank's cache (bf16 [N, 576], or uint8 e4m3 codes)."""
+    fp8 = kv_cache.dtype == torch.uint8
+    _check(lib().mla_write_kv(int(seq_lens.shape[0]), int(kv_new.shape[0]),
+                              _ptr(seq_lens, torch.int32, "seq_lens"),
+                              _ptr(qo_indptr, torch.int32, "qo_indptr"),
+                              _ptr(kv_new, torch.bfloat16, "kv_new"), int(world_size), int(rank),
+                              int(interleave), _ptr(block_table, torch.int32, "block_table"),
+                              int(block_table.shape[1]), int(num_blocks), int(block_size),
+                              _ptr(kv_cache, None, "kv_cache"),
+                              MLA_KV_FP8_E4M3 if fp8 else MLA_KV_BF16, float(kv_scale),
+                              int(kv_cache.numel() // D_QK), _stream(stream)), "mla_write_kv")
+    return kv_cache
 
 
 def get_device_error(stream=None) -> int:

@@ -83,6 +83,11 @@ def _load():
             lib.oracle_merge_segments.restype = None
             lib.oracle_merge_states.argtypes = [c_i64, c_int, f64p, f64p, f64p, f64p]
             lib.oracle_merge_states.restype = None
+            lib.oracle_e4m3_encode_rne_sat.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode_rne_sat.restype = ctypes.c_uint8
+            lib.oracle_write_kv.argtypes = [c_int, i32p, i32p, vp, c_int, c_int, i32p, c_int, c_int,
+                                            vp, c_int, ctypes.c_float, c_i64]
+            lib.oracle_write_kv.restype = c_int
             _lib = lib
     return _lib
 
@@ -302,3 +307,25 @@ def sharded_attention(qo_indptr, row_len_global, q_bits, kv, kv_scale, sm_scale,
         parts_lse.append(l)
     out, lse = merge_states(np.stack(parts_out), np.stack(parts_lse))
     return out, lse, parts_out, parts_lse
+
+
+def e4m3_encode(x: float) -> int:
+    """float32 value -> e4m3 code, round to nearest even, saturating at 448."""
+    return int(_load().oracle_e4m3_encode_rne_sat(float(x)))
+
+
+def write_kv(seq_lens, qo_indptr, kv_new_bits, world_size, rank, block_table, block_size,
+             cache, kv_scale=1.0):
+    """Owner-filtered paged write of the new verify tokens into one rank's cache
+    [sglang #34432, 实现拆解 4, set_mla_kv_buffer].  cache (uint16 bf16 bits or
+    uint8 e4m3 codes, [rows, 576]) is updated in place."""
+    seq, sp = _i32(seq_lens)
+    ind, ip = _i32(qo_indptr)
+    kvn = np.ascontiguousarray(kv_new_bits, dtype=np.uint16)
+    bt, bp = _i32(block_table)
+    assert cache.flags["C_CONTIGUOUS"] and cache.shape[1] == D_K
+    dt = 0 if cache.dtype == np.uint16 else 1
+    _check(_load().oracle_write_kv(seq.shape[0], sp, ip, kvn.ctypes.data, int(world_size), int(rank),
+                                   bp, bt.shape[1], int(block_size), cache.ctypes.data, dt,
+                                   float(kv_scale), cache.shape[0]), "write_kv")
+    return cache

@@ -43,6 +43,7 @@
 #define ORC_ERR_BLOCK 4
 #define ORC_ERR_UNSUPPORTED 5
 #define ORC_ERR_NOMEM 6
+#define ORC_ERR_SLOT 7
 
 int oracle_num_threads(void) {
 #ifdef _OPENMP
@@ -451,4 +452,71 @@ void oracle_merge_states(int64_t n_items, int num_parts,
     for (int d = 0; d < ORC_DV; d++) o[d] /= denom;
     lse[it] = M + log(denom);
   }
+}
+
+/* ------------------------------------------------------------------------ */
+/* e4m3 ("fn") encoding of a float32 value, round to nearest even with
+ * saturation to the largest finite magnitude 448 (NaN -> the NaN code 0x7F).
+ * Written from the format's definition: every non-negative finite code
+ * 0x00..0x7E is decoded with oracle_e4m3_to_double and the nearest one is
+ * chosen; on an exact tie the code with an even mantissa (even code) wins.  */
+uint8_t oracle_e4m3_encode_rne_sat(float xf) {
+  double x = (double)xf;
+  if (x != x) return 0x7F;
+  uint8_t sign = 0;
+  if (signbit(x)) { sign = 0x80; x = -x; }
+  if (x >= 448.0) return (uint8_t)(sign | 0x7E);
+  int best = 0;
+  double best_d = x;  /* distance to code 0 (value 0) */
+  for (int c = 1; c <= 0x7E; c++) {
+    double d = fabs(oracle_e4m3_to_double((uint8_t)c) - x);
+    if (d < best_d || (d == best_d && (c % 2) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* Owner-filtered paged KV write.  [sglang #34432, 实现拆解 4 and the
+ * forward_mla_rocm.py snippet: set_mla_kv_buffer writes the new tokens itself,
+ * filtering by owner and dividing by the shard count; key snippet
+ * g(j) = j * W + r].  Request b's qlen_b new tokens sit at global positions
+ * g = L_b - qlen_b + t (t < qlen_b; row qo_indptr[b] + t of kv_new).  Rank
+ * `rank` of W keeps the tokens with g mod W == rank, at its local index
+ * j = g div W, i.e. cache row block_table[b][j / block_size] * block_size +
+ * j % block_size.  bf16 caches receive the row's 576 bf16 values unchanged;
+ * fp8 caches receive e4m3 codes of (value / kv_scale) computed in float32
+ * (round to nearest even, saturating).  Returns 0 or an error code.          */
+int oracle_write_kv(int num_reqs, const int32_t *seq_lens, const int32_t *qo_indptr,
+                    const uint16_t *kv_new, int world_size, int rank,
+                    const int32_t *block_table, int bt_stride, int block_size, void *cache,
+                    int kv_dtype, float kv_scale, int64_t cache_rows) {
+  if (world_size < 1 || rank < 0 || rank >= world_size || block_size < 1) return ORC_ERR_ARG;
+  for (int b = 0; b < num_reqs; b++) {
+    int qlen = qo_indptr[b + 1] - qo_indptr[b];
+    int L = seq_lens[b];
+    if (qlen < 1 || qlen > L) return ORC_ERR_QLEN;
+    for (int t = 0; t < qlen; t++) {
+      int64_t g = (int64_t)L - qlen + t;
+      if (g % world_size != rank) continue;
+      int64_t j = g / world_size;
+      int32_t blk = block_table[(int64_t)b * bt_stride + j / block_size];
+      int64_t slot = (int64_t)blk * block_size + j % block_size;
+      if (blk < 0 || slot >= cache_rows) return ORC_ERR_SLOT;
+      const uint16_t *src = kv_new + (int64_t)(qo_indptr[b] + t) * ORC_DK;
+      for (int d = 0; d < ORC_DK; d++) {
+        if (kv_dtype == 0) {
+          ((uint16_t *)cache)[slot * ORC_DK + d] = src[d];
+        } else {
+          uint32_t u = ((uint32_t)src[d]) << 16;
+          float v;
+          memcpy(&v, &u, sizeof v);
+          float q = v / kv_scale; /* float32 division, as the kernel does */
+          ((uint8_t *)cache)[slot * ORC_DK + d] = oracle_e4m3_encode_rne_sat(q);
+        }
+      }
+    }
+  }
+  return ORC_OK;
 }
