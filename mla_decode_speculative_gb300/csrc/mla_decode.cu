@@ -405,6 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kRows, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kRows, 1, 1);
+      // Descriptors are built once; the start-address field (address >> 4 in
+      // the low 14 bits, addresses < 256 KB) is advanced with integer adds.
+      const uint64_t d_k0 = sdesc_sw128(s_slots, 0, 1024);                 // slot c: + c * 1024
+      const uint64_t d_q0 = sdesc_sw128(s_q, 0, 1024);                     // chunk c: + c * 512
+      const uint64_t d_v0 = sdesc_sw128(s_slots, kSlotBytes, 1024);         // block b: + b * 2048
+      const uint64_t d_p0 = sdesc_sw128(s_p, kSlotBytes, 1024);             // 16 tokens: + 128
+      const uint32_t t_s = tmem + kTmemS;
       uint32_t g = 0, kq = 0;
       bool ok = true;
       for (uint32_t k = 0; ok; ++k) {
@@ -426,12 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bar = smem_u32(kFp8 ? &misc.ready[c] : &misc.full[c]);
             if (!mbar_wait(bar, par, abort_flag, budget)) { fail(); ok = false; break; }
             tc_fence_after();
-            const uint32_t a0 = s_slots + c * kSlotBytes;
-            const uint32_t b0 = s_q + c * kQChunkBytes;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16_ss(tmem + kTmemS, sdesc_sw128(a0 + kk * 32, 0, 1024),
-                           sdesc_sw128(b0 + kk * 32, 0, 1024), idesc_qk, (c > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t da = d_k0 + static_cast<uint64_t>(c) * (kSlotBytes >> 4);
+            const uint64_t db = d_q0 + static_cast<uint64_t>(c) * (kQChunkBytes >> 4);
+            if (c == 0) umma_bf16_ss_first(t_s, da, db, idesc_qk);
+            else umma_bf16_ss_acc(t_s, da, db, idesc_qk);
+            umma_bf16_ss_acc(t_s, da + 2, db + 2, idesc_qk);  // +32 bytes along K
+            umma_bf16_ss_acc(t_s, da + 4, db + 4, idesc_qk);
+            umma_bf16_ss_acc(t_s, da + 6, db + 6, idesc_qk);
           }
           if (!ok) break;
           if (i == n_tiles - 1) umma_commit(smem_u32(&misc.q_empty));  // Q free for the next item
@@ -439,13 +447,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(smem_u32(&misc.p_full), par, abort_flag, budget)) { fail(); ok = false; break; }
           tc_fence_after();
           const int n_k16 = (n_valid + 15) / 16;
-#pragma unroll 1
+          // Block by block, so the first V slots are released after 8 UMMAs
+          // and the next tile's loads can start.  16 tokens = 2048 bytes of
+          // both operands.
+#pragma unroll
           for (int blk = 0; blk < 4; ++blk) {
-            const uint32_t a0 = s_slots + (2 * blk) * kSlotBytes;
-            for (int kk = 0; kk < n_k16; ++kk)
-              umma_bf16_ss(tmem + kTmemO + blk * kRows, sdesc_sw128(a0 + kk * 2048, kSlotBytes, 1024),
-                           sdesc_sw128(s_p + kk * 2048, kSlotBytes, 1024), idesc_pv,
-                           (i > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t t_o = tmem + kTmemO + blk * kRows;
+            const uint64_t da = d_v0 + static_cast<uint64_t>(blk) * ((2 * kSlotBytes) >> 4);
+            if (i == 0) umma_bf16_ss_first(t_o, da, d_p0, idesc_pv);
+            else umma_bf16_ss_acc(t_o, da, d_p0, idesc_pv);
+#pragma unroll
+            for (int kk = 1; kk < 8; ++kk)
+              if (kk < n_k16) umma_bf16_ss_acc(t_o, da + kk * 128, d_p0 + kk * 128, idesc_pv);
             umma_commit(smem_u32(&misc.empty[2 * blk]));
             umma_commit(smem_u32(&misc.empty[2 * blk + 1]));
           }
