@@ -13,28 +13,28 @@
 // GB300 design (not the pages' ROCm design):
 //  * Work item = (request, block of <= 64 query rows, split-K segment).  The
 //    rows of a request (heads x qlen) are decoded jointly against shared
-//    128-token KV tiles, so each latent row is read from HBM once per request
+//    64-token KV tiles, so each latent row is read from HBM once per request
 //    (the pages replicate the request once per verify row).
 //  * Persistent CTAs, one per SM.  The producer warp claims items from an
 //    atomic counter (dynamic load balance) and publishes each decoded item,
 //    with its rows' visible lengths, through a 4-deep shared-memory work
-//    ring; the next item's Q and first tile are loaded while the current
-//    item's epilogue runs.  Every barrier phase follows one running counter.
-//  * Swapped operand order, so every UMMA is M = 128 and the O accumulator
-//    fits TMEM densely:
-//        S^T[128 tok, 64 rows]   = K_tile[128, 576] . Q[64, 576]^T   (K-major A, K-major B)
-//        O^T[4x128 dims, 64 rows] += V^T[512, 128 tok] . P^T[64, 128]^T (MN-major A, MN-major B)
-//    TMEM: O^T in columns 0-255 (4 blocks x 64), S^T in columns 256-319.
-//  * Nine shared-memory slots of 128 tokens x 64 dims (16 KB, 128-byte
-//    swizzle): slot c holds chunk c of the tile (V chunks 0-7 stay where the
-//    PV operands need them adjacent), slot 8 the rope chunk; once the QK
-//    UMMAs have retired the rope chunk, slot 8 receives P^T for the PV UMMAs.
-//    All nine loads of a tile are issued as soon as the previous tile's PV
-//    frees the slots.  Q (64 x 576) is resident per item.
+//    ring.  Every barrier phase follows one running tile counter.
+//  * Swapped operand order, so the output accumulator fits TMEM densely:
+//        S^T[64 tok, 64 rows]     = K_tile[64, 576] . Q[64, 576]^T      (M = 64, K-major A and B)
+//        O^T[4x128 dims, 64 rows] += V^T[512, 64 tok] . P^T[64, 64]^T   (M = 128, MN-major A and B)
+//    TMEM: O^T in columns 0-255 (4 blocks x 64), S^T of stage s in columns
+//    256 + 64 s (an M = 64 result puts token 16 q + i in lane 32 q + i).
+//  * Two shared-memory stages of one 64-token tile each: nine 8 KB chunks of
+//    64 tokens x 64 dims (128-byte swizzle), the eight V chunks adjacent so
+//    PV reads them in place, the rope chunk last; once QK has retired a
+//    stage's rope chunk it receives that tile's P^T.  The UMMA warp issues
+//    QK of tile i + 1 before PV of tile i, so the loads of one stage and the
+//    QK of the next overlap the softmax of the current tile.  Q (64 x 576)
+//    is resident per item.
 //  * Warp roles: warps 0-7 softmax (column group g = warp / 4 owns rows
 //    32g..32g+31; TMEM lane quarter = warp % 4), warp 8 TMA producer, warp 9
 //    UMMA issuer and TMEM owner.  fp8 tiles are TMA-loaded into the upper
-//    half of a slot and expanded in place to bf16 by the softmax warps.
+//    half of each chunk and expanded in place to bf16 by the softmax warps.
 //  * Lazy rescaling: the running reference max only moves when a tile's max
 //    exceeds it by more than 2^8, so O is rarely rescaled in TMEM.
 //  * Every wait is bounded; a timeout records MLA_DEV_WAIT_TIMEOUT, lets all
@@ -54,25 +54,26 @@
 namespace mla {
 namespace {
 
-constexpr int kTileTok = 128;      // KV tokens per tile (UMMA M of the QK product)
+constexpr int kTileTok = 64;       // KV tokens per tile (UMMA M of the QK product)
 constexpr int kRows = 64;          // query rows per work item (UMMA N)
 constexpr int kNumChunks = 9;      // 576 / 64 dims per 128-byte swizzled chunk
-constexpr int kNumSlots = 9;       // chunk c -> slot c; slot 8: rope chunk, then P^T
-constexpr int kPSlot = 8;
-constexpr int kSlotBytes = kTileTok * 128;     // 16 KB
-constexpr int kQChunkBytes = kRows * 128;      // 8 KB
+constexpr int kStages = 2;         // tiles in flight
+constexpr int kPChunk = 8;         // rope chunk of a stage, then the tile's P^T
+constexpr int kChunkBytes = kTileTok * 128;            // 8 KB
+constexpr int kStageBytes = kNumChunks * kChunkBytes;  // 72 KB
+constexpr int kQChunkBytes = kRows * 128;              // 8 KB
 constexpr int kNumSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
-constexpr uint32_t kTmemS = 256;
+constexpr uint32_t kTmemS = 256;   // stage s: + 64 s
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
-constexpr int kOffSlots = 0;
-constexpr int kOffQ = kOffSlots + kNumSlots * kSlotBytes;
+constexpr int kOffStages = 0;
+constexpr int kOffQ = kOffStages + kStages * kStageBytes;
 constexpr int kOffMisc = kOffQ + kNumChunks * kQChunkBytes;
 
 // One claimed work item as published by the producer to the other roles.
@@ -84,10 +85,12 @@ struct WorkEntry {
 constexpr int kWorkRing = 4;
 
 struct Misc {
-  uint64_t full[kNumSlots];
-  uint64_t ready[kNumSlots];  // fp8 only: slot expanded to bf16
-  uint64_t empty[kNumSlots];
-  uint64_t q_full, q_empty, s_full, p_full, o_done, fin;
+  uint64_t full[kStages];
+  uint64_t ready[kStages];    // fp8 only: stage expanded to bf16
+  uint64_t empty[kStages];
+  uint64_t s_full[kStages];   // QK of the stage's tile retired
+  uint64_t p_full[kStages];   // P^T of the stage's tile written
+  uint64_t q_full, q_empty, o_done, fin;
   uint64_t work_full[kWorkRing], work_empty[kWorkRing];
   uint32_t tmem_base;
   int abort;
@@ -97,6 +100,7 @@ struct Misc {
 };
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc)) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kStageBytes % 1024 == 0 && kOffQ % 1024 == 0, "swizzle-atom alignment");
 
 struct Params {
   const int32_t *qo_indptr;
@@ -244,9 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Misc &misc = *reinterpret_cast<Misc *>(smem + kOffMisc);
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t s_slots = s_base + kOffSlots;
+  const uint32_t s_stage0 = s_base + kOffStages;   // stage s: + s * kStageBytes
   const uint32_t s_q = s_base + kOffQ;
-  const uint32_t s_p = s_slots + kPSlot * kSlotBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -260,15 +263,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumSlots; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&misc.full[i]), 1);
       mbar_init(smem_u32(&misc.ready[i]), kNumSoftmaxWarps);
       mbar_init(smem_u32(&misc.empty[i]), 1);
+      mbar_init(smem_u32(&misc.s_full[i]), 1);
+      mbar_init(smem_u32(&misc.p_full[i]), kNumSoftmaxWarps);
     }
     mbar_init(smem_u32(&misc.q_full), 1);
     mbar_init(smem_u32(&misc.q_empty), 1);
-    mbar_init(smem_u32(&misc.s_full), 1);
-    mbar_init(smem_u32(&misc.p_full), kNumSoftmaxWarps);
     mbar_init(smem_u32(&misc.o_done), 1);
     mbar_init(smem_u32(&misc.fin), 1);
     for (int i = 0; i < kWorkRing; ++i) {
@@ -293,18 +296,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ======================================================== producer warp
     // Claims work items (atomic counter), publishes them to the other roles
-    // through the work ring, and lane 0 issues the item's TMA loads.
+    // through the work ring, and issues the item's TMA loads: Q once, then
+    // every tile into the next free stage.
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_kv);
     }
-    // (Lane 0 waits and posts the expected bytes; every lane issues the TMA
-    // copies of the sub-page it owns.)
-    const int page_bytes = P * (kFp8 ? 64 : 128);
-    // A slot is refilled only after its previous contents were consumed, so
-    // at most one load per slot is in flight: remember the latest one.
+    // A tile is loaded as runs of `run` consecutive cache rows (one sub-page,
+    // or half of a 128-row sub-page), one box per run and chunk.
+    const int run = P < kTileTok ? P : kTileTok;
+    const int box_bytes = run * (kFp8 ? 64 : 128);
+    // A stage is refilled only after its previous tile was consumed, so at
+    // most one load per stage is in flight: remember the latest one.
     uint32_t armed = 0, armed_par = 0;
     uint32_t g = 0, kq = 0;  // running tile / Q-load counters
     bool ok = true;
@@ -361,35 +366,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < n_tiles && ok; ++i, ++g) {
           const int tok0 = seg_lo + i * kTileTok;
           const int n_valid = min(kTileTok, seg_hi - tok0);
-          const int n_pages = (n_valid + P - 1) / P;
-          // lane j owns sub-page j of the tile: one id fetch per tile, held in a register
-          int32_t my_row = 0;
-          if (lane < n_pages) {
-            const int32_t id = sp_row[tok0 / P + lane];
+          const int n_ops = ((n_valid + run - 1) / run) * kNumChunks;
+          const uint32_t st = g & 1u;
+          if (lane == 0 && !mbar_wait(smem_u32(&misc.empty[st]), ((g >> 1) & 1u) ^ 1u, abort_flag, budget)) {
+            fail();
+            ok = false;
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          const uint32_t fbar = smem_u32(&misc.full[st]);
+          if (lane == 0) mbar_arrive_expect_tx(fbar, n_ops * box_bytes);
+          __syncwarp();  // the expected bytes are posted before any copy can complete
+          const uint32_t dst0 = s_stage0 + st * kStageBytes + (kFp8 ? kChunkBytes / 2 : 0);
+          for (int o = lane; o < n_ops; o += 32) {
+            const int r = o / kNumChunks, c = o - r * kNumChunks;
+            const int t = tok0 + r * run;
+            const int32_t id = sp_row[t / P];
+            int32_t row;
             if (id < 0 || static_cast<int64_t>(id) * P + P > p.num_cache_rows) {
               record_error(p.err, MLA_DEV_BAD_SUBPAGE);
-              my_row = static_cast<int32_t>(p.num_cache_rows);  // out of range: zero fill
+              row = static_cast<int32_t>(p.num_cache_rows);  // out of range: zero fill
             } else {
-              my_row = id * P;
+              row = id * P + (t % P);
             }
+            tma_load_2d(dst0 + c * kChunkBytes + r * box_bytes, &tm_kv, fbar, c * 64, row, pol_kv);
           }
-          const uint32_t wpar = (g & 1u) ^ 1u;
-          for (int c = 0; c < kNumChunks; ++c) {
-            if (lane == 0 && !mbar_wait(smem_u32(&misc.empty[c]), wpar, abort_flag, budget)) {
-              fail();
-              ok = false;
-            }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-            const uint32_t fbar = smem_u32(&misc.full[c]);
-            if (lane == 0) mbar_arrive_expect_tx(fbar, n_pages * page_bytes);
-            __syncwarp();  // the expected bytes are posted before any copy can complete
-            const uint32_t dst = s_slots + c * kSlotBytes + (kFp8 ? kSlotBytes / 2 : 0);
-            if (lane < n_pages)
-              tma_load_2d(dst + lane * page_bytes, &tm_kv, fbar, c * 64, my_row, pol_kv);
-            armed |= 1u << c;
-            armed_par = (armed_par & ~(1u << c)) | ((g & 1u) << c);
-          }
+          armed |= 1u << st;
+          armed_par = (armed_par & ~(1u << st)) | (((g >> 1) & 1u) << st);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -397,43 +400,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && (!ok || *abort_flag)) {
       // Let the copies already issued land before the CTA's memory is released.
       const volatile int never = 0;
-      for (int c = 0; c < kNumSlots; ++c)
-        if (armed & (1u << c)) mbar_wait(smem_u32(&misc.full[c]), (armed_par >> c) & 1u, &never, budget);
+      for (int st = 0; st < kStages; ++st)
+        if (armed & (1u << st)) mbar_wait(smem_u32(&misc.full[st]), (armed_par >> st) & 1u, &never, budget);
     }
   } else if (warp == kMmaWarp) {
     // ======================================================== UMMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kRows, 0, 0);
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileTok, kRows, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kRows, 1, 1);
       // Descriptors are built once; the start-address field (address >> 4 in
       // the low 14 bits, addresses < 256 KB) is advanced with integer adds.
-      const uint64_t d_k0 = sdesc_sw128(s_slots, 0, 1024);                 // slot c: + c * 1024
-      const uint64_t d_q0 = sdesc_sw128(s_q, 0, 1024);                     // chunk c: + c * 512
-      const uint64_t d_v0 = sdesc_sw128(s_slots, kSlotBytes, 1024);         // block b: + b * 2048
-      const uint64_t d_p0 = sdesc_sw128(s_p, kSlotBytes, 1024);             // 16 tokens: + 128
-      const uint32_t t_s = tmem + kTmemS;
+      //   K chunk c of stage s:  d_k0 + s * 4608 + c * 512   (+2 per 16 dims)
+      //   Q chunk c:             d_q0 + c * 512
+      //   V^T block b:           d_v0 + s * 4608 + b * 1024  (LBO: next 64-dim chunk; +128 per 16 tokens)
+      //   P^T (rope chunk):      d_p0 + s * 4608             (+128 per 16 tokens)
+      constexpr uint32_t kStageDesc = kStageBytes >> 4;
+      const uint64_t d_k0 = sdesc_sw128(s_stage0, 0, 1024);
+      const uint64_t d_q0 = sdesc_sw128(s_q, 0, 1024);
+      const uint64_t d_v0 = sdesc_sw128(s_stage0, kChunkBytes, 1024);
+      const uint64_t d_p0 = sdesc_sw128(s_stage0 + kPChunk * kChunkBytes, kChunkBytes, 1024);
       uint32_t g = 0, kq = 0;
+      // PV of a tile is issued after the QK of the next tile of the item
+      // (the softmax of the tile runs meanwhile): the pending tile's counter
+      // and shape.
+      bool pend = false, pend_first = false;
+      uint32_t pend_g = 0;
+      int pend_k16 = 0;
       bool ok = true;
+      auto issue_pv = [&]() -> bool {
+        const uint32_t st = pend_g & 1u;
+        if (!mbar_wait(smem_u32(&misc.p_full[st]), (pend_g >> 1) & 1u, abort_flag, budget)) return false;
+        tc_fence_after();
+        const uint64_t dv = d_v0 + st * kStageDesc, dp = d_p0 + st * kStageDesc;
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          const uint32_t t_o = tmem + kTmemO + blk * kRows;
+          const uint64_t da = dv + static_cast<uint64_t>(blk) * ((2 * kChunkBytes) >> 4);
+          if (pend_first) umma_bf16_ss_first(t_o, da, dp, idesc_pv);
+          else umma_bf16_ss_acc(t_o, da, dp, idesc_pv);
+#pragma unroll
+          for (int kk = 1; kk < kTileTok / 16; ++kk)
+            if (kk < pend_k16) umma_bf16_ss_acc(t_o, da + kk * 128, dp + kk * 128, idesc_pv);
+        }
+        umma_commit(smem_u32(&misc.empty[st]));  // stage (V and P^T) free for the next load
+        umma_commit(smem_u32(&misc.o_done));
+        return true;
+      };
       for (uint32_t k = 0; ok; ++k) {
         const uint32_t ws = k % kWorkRing;
-        if (!mbar_wait(smem_u32(&misc.work_full[ws]), (k / kWorkRing) & 1u, abort_flag, budget)) { fail(); break; }
+        if (!mbar_wait(smem_u32(&misc.work_full[ws]), (k / kWorkRing) & 1u, abort_flag, budget)) { fail(); ok = false; break; }
         const WorkEntry &e = misc.work[ws];
         const int w = e.w;
         const int n_tiles = e.n_tiles, seg_lo = e.seg_lo, seg_hi = e.seg_hi;
         if (w >= 0) mbar_arrive(smem_u32(&misc.work_empty[ws]));
         if (w < 0) break;
         if (n_tiles == 0) continue;
-        if (!mbar_wait(smem_u32(&misc.q_full), kq & 1u, abort_flag, budget)) { fail(); break; }
+        if (!mbar_wait(smem_u32(&misc.q_full), kq & 1u, abort_flag, budget)) { fail(); ok = false; break; }
         ++kq;
         tc_fence_after();
         for (int i = 0; i < n_tiles; ++i, ++g) {
           const int n_valid = min(kTileTok, seg_hi - (seg_lo + i * kTileTok));
-          const uint32_t par = g & 1u;
+          const uint32_t st = g & 1u;
+          const uint32_t bar = smem_u32(kFp8 ? &misc.ready[st] : &misc.full[st]);
+          if (!mbar_wait(bar, (g >> 1) & 1u, abort_flag, budget)) { fail(); ok = false; break; }
+          tc_fence_after();
+          const uint32_t t_s = tmem + kTmemS + st * 64;
+          const uint64_t dk = d_k0 + st * kStageDesc;
+#pragma unroll
           for (int c = 0; c < kNumChunks; ++c) {
-            const uint32_t bar = smem_u32(kFp8 ? &misc.ready[c] : &misc.full[c]);
-            if (!mbar_wait(bar, par, abort_flag, budget)) { fail(); ok = false; break; }
-            tc_fence_after();
-            const uint64_t da = d_k0 + static_cast<uint64_t>(c) * (kSlotBytes >> 4);
+            const uint64_t da = dk + static_cast<uint64_t>(c) * (kChunkBytes >> 4);
             const uint64_t db = d_q0 + static_cast<uint64_t>(c) * (kQChunkBytes >> 4);
             if (c == 0) umma_bf16_ss_first(t_s, da, db, idesc_qk);
             else umma_bf16_ss_acc(t_s, da, db, idesc_qk);
@@ -441,29 +476,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16_ss_acc(t_s, da + 4, db + 4, idesc_qk);
             umma_bf16_ss_acc(t_s, da + 6, db + 6, idesc_qk);
           }
-          if (!ok) break;
           if (i == n_tiles - 1) umma_commit(smem_u32(&misc.q_empty));  // Q free for the next item
-          umma_commit(smem_u32(&misc.s_full));
-          if (!mbar_wait(smem_u32(&misc.p_full), par, abort_flag, budget)) { fail(); ok = false; break; }
-          tc_fence_after();
-          const int n_k16 = (n_valid + 15) / 16;
-          // Block by block, so the first V slots are released after 8 UMMAs
-          // and the next tile's loads can start.  16 tokens = 2048 bytes of
-          // both operands.
-#pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            const uint32_t t_o = tmem + kTmemO + blk * kRows;
-            const uint64_t da = d_v0 + static_cast<uint64_t>(blk) * ((2 * kSlotBytes) >> 4);
-            if (i == 0) umma_bf16_ss_first(t_o, da, d_p0, idesc_pv);
-            else umma_bf16_ss_acc(t_o, da, d_p0, idesc_pv);
-#pragma unroll
-            for (int kk = 1; kk < 8; ++kk)
-              if (kk < n_k16) umma_bf16_ss_acc(t_o, da + kk * 128, d_p0 + kk * 128, idesc_pv);
-            umma_commit(smem_u32(&misc.empty[2 * blk]));
-            umma_commit(smem_u32(&misc.empty[2 * blk + 1]));
-          }
-          umma_commit(smem_u32(&misc.empty[kPSlot]));  // P consumed: slot 8 may take the next rope
-          umma_commit(smem_u32(&misc.o_done));
+          umma_commit(smem_u32(&misc.s_full[st]));
+          if (pend && !issue_pv()) { fail(); ok = false; break; }
+          pend = true;
+          pend_g = g;
+          pend_first = (i == 0);
+          pend_k16 = (n_valid + 15) / 16;
+        }
+        // The item's last PV is not deferred: its epilogue waits for it, and
+        // the next item's first QK waits for that item's Q load anyway.
+        if (ok && pend) {
+          pend = false;
+          if (!issue_pv()) { fail(); ok = false; }
         }
       }
       umma_commit(smem_u32(&misc.fin));
@@ -474,7 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================================================== softmax warps
     const int g_col = warp >> 2;       // column group: rows 32g .. 32g+31 of the block
     const int wq = warp & 3;           // TMEM lane quarter
-    const int tok = wq * 32 + lane;    // token row of S^T (and dim row of an O^T block)
+    const bool s_lane = lane < 16;     // lanes 0-15 of a quarter hold S^T rows (M = 64)
+    const int tok = wq * 16 + (lane & 15);  // token row of S^T handled by this lane
+    const int dim_lane = wq * 32 + lane;    // dim row of an O^T block
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     const int my_col = 32 * g_col + lane;  // column whose statistics this lane keeps
     int red_buf = 0;
@@ -526,48 +553,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_tiles; ++i, ++g) {
         const int tok0 = seg_lo + i * kTileTok;
         const int n_valid = min(kTileTok, seg_hi - tok0);
-        const uint32_t par = g & 1u;
+        const uint32_t st = g & 1u;
+        const uint32_t par = (g >> 1) & 1u;
+        const uint32_t s_stage = s_stage0 + st * kStageBytes;
 
         if constexpr (kFp8) {
-          // Expand this tile's nine fp8 chunks to bf16 in place, in load order.
-          const int t2 = threadIdx.x >> 1;  // token row 0..127
-          const int hf = threadIdx.x & 1;   // which 32 of the 64 dims
-          for (int c = 0; c < kNumChunks; ++c) {
-            if (ok && !mbar_wait(smem_u32(&misc.full[c]), par, abort_flag, budget)) {
-              fail();
-              ok = false;
-            }
-            const uint32_t slot = s_slots + c * kSlotBytes;
-            const uint4 c0 = ld_shared_v4(slot + kSlotBytes / 2 + t2 * 64 + hf * 32);
-            const uint4 c1 = ld_shared_v4(slot + kSlotBytes / 2 + t2 * 64 + hf * 32 + 16);
-            named_bar_sync(3, kNumSoftmaxWarps * 32);
-            const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t lo = wv[2 * q], hi = wv[2 * q + 1];
-              const uint32_t chunk = static_cast<uint32_t>((hf * 4 + q) ^ (t2 & 7));
-              st_shared_v4(slot + t2 * 128 + chunk * 16, e4m3x2_to_bf16x2(lo & 0xffff),
-                           e4m3x2_to_bf16x2(lo >> 16), e4m3x2_to_bf16x2(hi & 0xffff),
-                           e4m3x2_to_bf16x2(hi >> 16));
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&misc.ready[c]));
+          // Expand the stage's nine fp8 chunks to bf16 in place: every
+          // thread reads its 16 codes of each chunk, then all write.
+          if (ok && !mbar_wait(smem_u32(&misc.full[st]), par, abort_flag, budget)) {
+            fail();
+            ok = false;
           }
+          const int t4 = threadIdx.x >> 2;  // token row 0..63
+          const int qt = threadIdx.x & 3;   // which 16 of the 64 dims
+          uint4 raw[kNumChunks];
+#pragma unroll
+          for (int c = 0; c < kNumChunks; ++c)
+            raw[c] = ld_shared_v4(s_stage + c * kChunkBytes + kChunkBytes / 2 + t4 * 64 + qt * 16);
+          named_bar_sync(3, kNumSoftmaxWarps * 32);
+#pragma unroll
+          for (int c = 0; c < kNumChunks; ++c) {
+            const uint32_t row_addr = s_stage + c * kChunkBytes + t4 * 128;
+            const uint32_t c0 = static_cast<uint32_t>((2 * qt) ^ (t4 & 7));
+            const uint32_t c1 = static_cast<uint32_t>((2 * qt + 1) ^ (t4 & 7));
+            st_shared_v4(row_addr + c0 * 16, e4m3x2_to_bf16x2(raw[c].x & 0xffff), e4m3x2_to_bf16x2(raw[c].x >> 16),
+                         e4m3x2_to_bf16x2(raw[c].y & 0xffff), e4m3x2_to_bf16x2(raw[c].y >> 16));
+            st_shared_v4(row_addr + c1 * 16, e4m3x2_to_bf16x2(raw[c].z & 0xffff), e4m3x2_to_bf16x2(raw[c].z >> 16),
+                         e4m3x2_to_bf16x2(raw[c].w & 0xffff), e4m3x2_to_bf16x2(raw[c].w >> 16));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&misc.ready[st]));
         }
 
-        if (ok && !mbar_wait(smem_u32(&misc.s_full), par, abort_flag, budget)) {
+        if (ok && !mbar_wait(smem_u32(&misc.s_full[st]), par, abort_flag, budget)) {
           fail();
           ok = false;
         }
         tc_fence_after();
         uint32_t sv[32];
-        tmem_ld32(tmem + lane_addr + kTmemS + 32 * g_col, sv);
+        tmem_ld32(tmem + lane_addr + kTmemS + st * 64 + 32 * g_col, sv);
 
         // scaled scores (log2 units), causal + segment mask per column
         float x[32];
         const int gtok = tok0 + tok;
-        const bool tok_in = tok < n_valid;
+        const bool tok_in = s_lane && tok < n_valid;
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
           const int4 lens = *reinterpret_cast<const int4 *>(&lens_g[4 * j4]);
@@ -616,16 +646,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) l_part[j] += x[j];
 
-        // The previous tile's PV (possibly of the previous item) must be done
-        // before P (slot 8) and O are touched.
-        if (g > 0) {
+        // P^T row `tok`, columns 32g .. 32g+31 (bf16, 128-byte swizzle), into
+        // the stage's rope chunk (the tile's QK has retired it).
+        const uint32_t s_pt = s_stage + kPChunk * kChunkBytes;
+        if (s_lane) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t chunk = static_cast<uint32_t>((4 * g_col + q) ^ (tok & 7));
+            st_shared_v4(s_pt + tok * 128 + chunk * 16, pack_bf16(x[8 * q + 0], x[8 * q + 1]),
+                         pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
+                         pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+          }
+          // V rows past the last valid token but inside the last 16-token MMA
+          // step hold stale or foreign data: zero them so 0 * V stays 0.
+          if (tok >= n_valid && tok < ((n_valid + 15) & ~15)) {
+            for (int c = 4 * g_col; c < 4 * g_col + 4; ++c)
+#pragma unroll
+              for (int c16 = 0; c16 < 8; ++c16)
+                st_shared_v4(s_stage + c * kChunkBytes + tok * 128 + c16 * 16, 0, 0, 0, 0);
+          }
+        }
+        // O is rescaled in TMEM only after the previous tile's PV retired.
+        if (i > 0 && any_rescale) {
           if (ok && !mbar_wait(smem_u32(&misc.o_done), (g - 1) & 1u, abort_flag, budget)) {
             fail();
             ok = false;
           }
           tc_fence_after();
-        }
-        if (i > 0 && any_rescale) {
 #pragma unroll 1
           for (int blk = 0; blk < 4; ++blk) {
             const uint32_t taddr = tmem + lane_addr + kTmemO + blk * kRows + 32 * g_col;
@@ -637,26 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(taddr, ov);
           }
         }
-        // P^T row `tok`, columns 32g .. 32g+31 (bf16, 128-byte swizzle), into slot 8
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t chunk = static_cast<uint32_t>((4 * g_col + q) ^ (tok & 7));
-          st_shared_v4(s_p + tok * 128 + chunk * 16, pack_bf16(x[8 * q + 0], x[8 * q + 1]),
-                       pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
-                       pack_bf16(x[8 * q + 6], x[8 * q + 7]));
-        }
-        // V rows past the last valid token but inside the last 16-token MMA step
-        // hold stale or foreign data: zero them so 0 * V stays 0.
-        if (!tok_in && tok < ((n_valid + 15) & ~15)) {
-          for (int sl = 4 * g_col; sl < 4 * g_col + 4; ++sl)
-#pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16)
-              st_shared_v4(s_slots + sl * kSlotBytes + tok * 128 + c16 * 16, 0, 0, 0, 0);
-        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&misc.p_full));
+        if (lane == 0) mbar_arrive(smem_u32(&misc.p_full[st]));
       }
 
       // ---- epilogue of the item: row sums, statistics, output
@@ -693,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ov[32];
         tmem_ld32(tmem + lane_addr + kTmemO + blk * kRows + 32 * g_col, ov);
         if (!write) continue;
-        const int dim = blk * 128 + tok;
+        const int dim = blk * 128 + dim_lane;
         if (direct) {
           __nv_bfloat16 *o = p.out + r0 * 512 + dim;
 #pragma unroll
@@ -734,13 +765,14 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
                                static_cast<uint64_t>(a.num_rows) * a.num_heads, 64, kRows,
                                CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != MLA_OK) return st;
+  const int box_rows = a.page_size < kTileTok ? a.page_size : kTileTok;  // one run of a tile
   if (fp8)
     st = make_tmap_2d(&tm_kv, a.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 576,
-                      static_cast<uint64_t>(a.num_cache_rows), 64, a.page_size,
+                      static_cast<uint64_t>(a.num_cache_rows), 64, box_rows,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   else
     st = make_tmap_2d(&tm_kv, a.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 576,
-                      static_cast<uint64_t>(a.num_cache_rows), 64, a.page_size,
+                      static_cast<uint64_t>(a.num_cache_rows), 64, box_rows,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != MLA_OK) return st;
 
