@@ -212,6 +212,34 @@ mla_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType 
   return MLA_OK;
 }
 
+mla_status make_tmap_tile3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                            int elem_bytes, uint64_t rows, uint32_t box_rows,
+                            CUtensorMapSwizzle swizzle) {
+  // A latent row of 576 values seen as 9 chunks of 64: dims (64 values, row,
+  // chunk) with strides (row = 576 values, chunk = 64 values), so one box of
+  // (64, box_rows, 9) lands chunk-major in shared memory: chunk c at
+  // c * box_rows * 64 * elem_bytes, rows inside a chunk contiguous.
+  if (g_encode == nullptr) {
+    CUtensorMap scratch;
+    const mla_status st = make_tmap_2d(&scratch, base, dtype, elem_bytes, 576, rows, 64, 8, swizzle);
+    if (st != MLA_OK) return st;
+  }
+  const uint64_t eb = static_cast<uint64_t>(elem_bytes);
+  const cuuint64_t dims[3] = {64, rows, 9};
+  const cuuint64_t strides[2] = {576 * eb, 64 * eb};
+  const cuuint32_t box[3] = {64, box_rows, 9};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (3-D tile view) failed (CUresult %d): rows=%llu box_rows=%u", (int)r,
+              (unsigned long long)rows, box_rows);
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
 mla_status launch_plan_rows(int B, int T, const int32_t *seq_lens, const int32_t *ind,
                             int32_t *row_len, int32_t *row_req, const TableLaunch &t,
                             int *err, cudaStream_t stream) {

@@ -124,6 +124,7 @@ struct Params {
   int max_qlen;
   int num_rows;
   int max_len;
+  int tile3d;              // KV tensor map is the 3-D whole-tile view (page size >= 64)
   float score_scale_log2;  // sm_scale * kv_scale * log2(e)
   float out_scale;         // kv_scale (fp8) or 1
 };
@@ -306,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // A tile is loaded as runs of `run` consecutive cache rows (one sub-page,
     // or half of a 128-row sub-page), one box per run and chunk.
+    const bool tile3d = p.tile3d != 0;
     const int run = P < kTileTok ? P : kTileTok;
     const int box_bytes = run * (kFp8 ? 64 : 128);
     // A stage is refilled only after its previous tile was consumed, so at
@@ -347,6 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_tiles = __shfl_sync(0xffffffffu, lane == 0 ? e.n_tiles : 0, 0);
       if (n_tiles > 0) {
         const int seg_lo = e.seg_lo, seg_hi = e.seg_hi, row_base = e.row_base;
+        // Sub-page ids are read 32 at a time (lane l holds page win_base + l),
+        // ahead of the waits, so no id fetch sits between a freed stage and
+        // its next copies.
+        const int32_t *sp_row = p.subpage_table + static_cast<int64_t>(e.b) * p.subpage_stride;
+        const int last_page = (seg_hi - 1) / P;
+        int win_base = seg_lo / P;
+        int32_t win_id = (win_base + lane <= last_page) ? sp_row[win_base + lane] : -1;
         // Q of this item, once the previous item's last QK is done with the buffer
         if (lane == 0 && ok &&
             !mbar_wait(smem_u32(&misc.q_empty), (kq & 1u) ^ 1u, abort_flag, budget)) {
@@ -362,12 +371,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(s_q + lane * kQChunkBytes, &tm_q, q_bar, lane * 64, row_base, pol_q);
         }
         ++kq;
-        const int32_t *sp_row = p.subpage_table + static_cast<int64_t>(e.b) * p.subpage_stride;
         for (int i = 0; i < n_tiles && ok; ++i, ++g) {
           const int tok0 = seg_lo + i * kTileTok;
           const int n_valid = min(kTileTok, seg_hi - tok0);
           const int n_ops = ((n_valid + run - 1) / run) * kNumChunks;
           const uint32_t st = g & 1u;
+          if ((tok0 + n_valid - 1) / P >= win_base + 32) {  // warp-uniform: slide the id window
+            win_base = tok0 / P;
+            win_id = (win_base + lane <= last_page) ? sp_row[win_base + lane] : -1;
+          }
           if (lane == 0 && !mbar_wait(smem_u32(&misc.empty[st]), ((g >> 1) & 1u) ^ 1u, abort_flag, budget)) {
             fail();
             ok = false;
@@ -375,21 +387,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
           const uint32_t fbar = smem_u32(&misc.full[st]);
+          // fp8 codes land packed in the stage's upper half (chunk c at c * 4 KB)
+          const uint32_t dst0 = s_stage0 + st * kStageBytes + (kFp8 ? kStageBytes / 2 : 0);
+          if (tile3d) {
+            // P >= 64: the tile is 64 consecutive rows of one sub-page, one 3-D box
+            const int32_t id = __shfl_sync(0xffffffffu, win_id, tok0 / P - win_base);
+            if (lane == 0) {
+              int32_t row;
+              if (id < 0 || static_cast<int64_t>(id) * P + P > p.num_cache_rows) {
+                record_error(p.err, MLA_DEV_BAD_SUBPAGE);
+                row = static_cast<int32_t>(p.num_cache_rows);  // out of range: zero fill
+              } else {
+                row = id * P + (tok0 % P);
+              }
+              mbar_arrive_expect_tx(fbar, kFp8 ? kStageBytes / 2 : kStageBytes);
+              tma_load_3d(dst0, &tm_kv, fbar, 0, row, 0, pol_kv);
+            }
+            armed |= 1u << st;
+            armed_par = (armed_par & ~(1u << st)) | (((g >> 1) & 1u) << st);
+            continue;
+          }
           if (lane == 0) mbar_arrive_expect_tx(fbar, n_ops * box_bytes);
           __syncwarp();  // the expected bytes are posted before any copy can complete
-          const uint32_t dst0 = s_stage0 + st * kStageBytes + (kFp8 ? kChunkBytes / 2 : 0);
-          for (int o = lane; o < n_ops; o += 32) {
+          for (int o0 = 0; o0 < n_ops; o0 += 32) {  // uniform trip count (the shuffle needs every lane)
+            const int o = o0 + lane;
             const int r = o / kNumChunks, c = o - r * kNumChunks;
             const int t = tok0 + r * run;
-            const int32_t id = sp_row[t / P];
-            int32_t row;
-            if (id < 0 || static_cast<int64_t>(id) * P + P > p.num_cache_rows) {
-              record_error(p.err, MLA_DEV_BAD_SUBPAGE);
-              row = static_cast<int32_t>(p.num_cache_rows);  // out of range: zero fill
-            } else {
-              row = id * P + (t % P);
+            const int src = o < n_ops ? t / P - win_base : 0;
+            const int32_t id = __shfl_sync(0xffffffffu, win_id, src);
+            if (o < n_ops) {
+              int32_t row;
+              if (id < 0 || static_cast<int64_t>(id) * P + P > p.num_cache_rows) {
+                record_error(p.err, MLA_DEV_BAD_SUBPAGE);
+                row = static_cast<int32_t>(p.num_cache_rows);  // out of range: zero fill
+              } else {
+                row = id * P + (t % P);
+              }
+              tma_load_2d(dst0 + c * (kFp8 ? kChunkBytes / 2 : kChunkBytes) + r * box_bytes, &tm_kv, fbar,
+                          c * 64, row, pol_kv);
             }
-            tma_load_2d(dst0 + c * kChunkBytes + r * box_bytes, &tm_kv, fbar, c * 64, row, pol_kv);
           }
           armed |= 1u << st;
           armed_par = (armed_par & ~(1u << st)) | (((g >> 1) & 1u) << st);
@@ -419,51 +455,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t d_q0 = sdesc_sw128(s_q, 0, 1024);
       const uint64_t d_v0 = sdesc_sw128(s_stage0, kChunkBytes, 1024);
       const uint64_t d_p0 = sdesc_sw128(s_stage0 + kPChunk * kChunkBytes, kChunkBytes, 1024);
-      uint32_t g = 0, kq = 0;
-      // PV of a tile is issued after the QK of the next tile of the item
-      // (the softmax of the tile runs meanwhile): the pending tile's counter
-      // and shape.
-      bool pend = false, pend_first = false;
-      uint32_t pend_g = 0;
-      int pend_k16 = 0;
-      bool ok = true;
-      auto issue_pv = [&]() -> bool {
-        const uint32_t st = pend_g & 1u;
-        if (!mbar_wait(smem_u32(&misc.p_full[st]), (pend_g >> 1) & 1u, abort_flag, budget)) return false;
-        tc_fence_after();
-        const uint64_t dv = d_v0 + st * kStageDesc, dp = d_p0 + st * kStageDesc;
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          const uint32_t t_o = tmem + kTmemO + blk * kRows;
-          const uint64_t da = dv + static_cast<uint64_t>(blk) * ((2 * kChunkBytes) >> 4);
-          if (pend_first) umma_bf16_ss_first(t_o, da, dp, idesc_pv);
-          else umma_bf16_ss_acc(t_o, da, dp, idesc_pv);
-#pragma unroll
-          for (int kk = 1; kk < kTileTok / 16; ++kk)
-            if (kk < pend_k16) umma_bf16_ss_acc(t_o, da + kk * 128, dp + kk * 128, idesc_pv);
-        }
-        umma_commit(smem_u32(&misc.empty[st]));  // stage (V and P^T) free for the next load
-        umma_commit(smem_u32(&misc.o_done));
-        return true;
-      };
-      for (uint32_t k = 0; ok; ++k) {
-        const uint32_t ws = k % kWorkRing;
-        if (!mbar_wait(smem_u32(&misc.work_full[ws]), (k / kWorkRing) & 1u, abort_flag, budget)) { fail(); ok = false; break; }
-        const WorkEntry &e = misc.work[ws];
-        const int w = e.w;
-        const int n_tiles = e.n_tiles, seg_lo = e.seg_lo, seg_hi = e.seg_hi;
-        if (w >= 0) mbar_arrive(smem_u32(&misc.work_empty[ws]));
-        if (w < 0) break;
-        if (n_tiles == 0) continue;
-        if (!mbar_wait(smem_u32(&misc.q_full), kq & 1u, abort_flag, budget)) { fail(); ok = false; break; }
-        ++kq;
-        tc_fence_after();
-        for (int i = 0; i < n_tiles; ++i, ++g) {
-          const int n_valid = min(kTileTok, seg_hi - (seg_lo + i * kTileTok));
-          const uint32_t st = g & 1u;
-          const uint32_t bar = smem_u32(kFp8 ? &misc.ready[st] : &misc.full[st]);
-          if (!mbar_wait(bar, (g >> 1) & 1u, abort_flag, budget)) { fail(); ok = false; break; }
+      // Event loop: PV of the oldest tile whose P^T is ready goes first (it
+      // frees that tile's stage for the next load); otherwise the next work
+      // entry, the item's Q, or QK of the item's next tile once its data has
+      // landed and an S^T buffer is free (at most two tiles between QK and
+      // PV).  Polling uses non-blocking barrier tests.
+      uint32_t gq = 0, gp = 0, kq = 0, k = 0;  // tiles QK'd / PV'd, Q loads, work entries
+      uint32_t first_bits = 0, k16_bits = 0;   // per S^T buffer: first tile of its item, 16-token steps
+      int it_left = 0, it_i = 0, it_lo = 0, it_hi = 0;
+      bool q_ready = false, no_more = false;
+      long long idle_since = clock64();
+      while (true) {
+        bool progress = true;
+        if (gp < gq && mbar_test(smem_u32(&misc.p_full[gp & 1u]), (gp >> 1) & 1u)) {
           tc_fence_after();
+          const uint32_t st = gp & 1u;
+          const bool first = (first_bits >> st) & 1u;
+          const int n_k16 = static_cast<int>((k16_bits >> (4 * st)) & 15u);
+          const uint64_t dv = d_v0 + st * kStageDesc, dp = d_p0 + st * kStageDesc;
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            const uint32_t t_o = tmem + kTmemO + blk * kRows;
+            const uint64_t da = dv + static_cast<uint64_t>(blk) * ((2 * kChunkBytes) >> 4);
+            if (first) umma_bf16_ss_first(t_o, da, dp, idesc_pv);
+            else umma_bf16_ss_acc(t_o, da, dp, idesc_pv);
+#pragma unroll
+            for (int kk = 1; kk < kTileTok / 16; ++kk)
+              if (kk < n_k16) umma_bf16_ss_acc(t_o, da + kk * 128, dp + kk * 128, idesc_pv);
+          }
+          umma_commit(smem_u32(&misc.empty[st]));  // stage (V and P^T) free for the next load
+          umma_commit(smem_u32(&misc.o_done));
+          ++gp;
+        } else if (it_left == 0 && !no_more) {
+          const uint32_t ws = k % kWorkRing;
+          if (mbar_test(smem_u32(&misc.work_full[ws]), (k / kWorkRing) & 1u)) {
+            const WorkEntry &e = misc.work[ws];
+            const int w = e.w;
+            it_left = w >= 0 ? e.n_tiles : 0;
+            it_lo = e.seg_lo;
+            it_hi = e.seg_hi;
+            it_i = 0;
+            q_ready = false;
+            if (w >= 0) mbar_arrive(smem_u32(&misc.work_empty[ws]));
+            else no_more = true;
+            ++k;
+          } else {
+            progress = false;
+          }
+        } else if (it_left > 0 && !q_ready) {
+          if (mbar_test(smem_u32(&misc.q_full), kq & 1u)) {
+            ++kq;
+            q_ready = true;
+            tc_fence_after();
+          } else {
+            progress = false;
+          }
+        } else if (it_left > 0 && gq - gp < 2 &&
+                   mbar_test(smem_u32(kFp8 ? &misc.ready[gq & 1u] : &misc.full[gq & 1u]), (gq >> 1) & 1u)) {
+          tc_fence_after();
+          const uint32_t st = gq & 1u;
           const uint32_t t_s = tmem + kTmemS + st * 64;
           const uint64_t dk = d_k0 + st * kStageDesc;
 #pragma unroll
@@ -476,19 +526,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16_ss_acc(t_s, da + 4, db + 4, idesc_qk);
             umma_bf16_ss_acc(t_s, da + 6, db + 6, idesc_qk);
           }
-          if (i == n_tiles - 1) umma_commit(smem_u32(&misc.q_empty));  // Q free for the next item
+          if (it_left == 1) umma_commit(smem_u32(&misc.q_empty));  // Q free for the next item
           umma_commit(smem_u32(&misc.s_full[st]));
-          if (pend && !issue_pv()) { fail(); ok = false; break; }
-          pend = true;
-          pend_g = g;
-          pend_first = (i == 0);
-          pend_k16 = (n_valid + 15) / 16;
+          const int n_valid = min(kTileTok, it_hi - (it_lo + it_i * kTileTok));
+          first_bits = (first_bits & ~(1u << st)) | (static_cast<uint32_t>(it_i == 0) << st);
+          k16_bits = (k16_bits & ~(15u << (4 * st))) | (static_cast<uint32_t>((n_valid + 15) / 16) << (4 * st));
+          ++gq;
+          ++it_i;
+          --it_left;
+        } else {
+          progress = false;
         }
-        // The item's last PV is not deferred: its epilogue waits for it, and
-        // the next item's first QK waits for that item's Q load anyway.
-        if (ok && pend) {
-          pend = false;
-          if (!issue_pv()) { fail(); ok = false; }
+        if (no_more && it_left == 0 && gp == gq) break;
+        if (progress) {
+          idle_since = clock64();
+        } else if (*abort_flag || clock64() - idle_since > budget) {
+          fail();
+          break;
         }
       }
       umma_commit(smem_u32(&misc.fin));
@@ -558,8 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_stage = s_stage0 + st * kStageBytes;
 
         if constexpr (kFp8) {
-          // Expand the stage's nine fp8 chunks to bf16 in place: every
-          // thread reads its 16 codes of each chunk, then all write.
+          // Expand the stage's nine fp8 chunks (packed in its upper half) to
+          // bf16 in place: every thread reads its 16 codes of each chunk,
+          // then all write.
           if (ok && !mbar_wait(smem_u32(&misc.full[st]), par, abort_flag, budget)) {
             fail();
             ok = false;
@@ -569,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4 raw[kNumChunks];
 #pragma unroll
           for (int c = 0; c < kNumChunks; ++c)
-            raw[c] = ld_shared_v4(s_stage + c * kChunkBytes + kChunkBytes / 2 + t4 * 64 + qt * 16);
+            raw[c] = ld_shared_v4(s_stage + kStageBytes / 2 + c * (kChunkBytes / 2) + t4 * 64 + qt * 16);
           named_bar_sync(3, kNumSoftmaxWarps * 32);
 #pragma unroll
           for (int c = 0; c < kNumChunks; ++c) {
@@ -666,13 +721,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st_shared_v4(s_stage + c * kChunkBytes + tok * 128 + c16 * 16, 0, 0, 0, 0);
           }
         }
-        // O is rescaled in TMEM only after the previous tile's PV retired.
-        if (i > 0 && any_rescale) {
+        // PV of the previous tile must have retired before O is rescaled,
+        // and in any case before this tile's P^T is released: o_done is then
+        // observed phase by phase (a parity wait cannot tell phases two
+        // apart), and the epilogue's wait covers every PV of the item.
+        if (g > 0) {
           if (ok && !mbar_wait(smem_u32(&misc.o_done), (g - 1) & 1u, abort_flag, budget)) {
             fail();
             ok = false;
           }
           tc_fence_after();
+        }
+        if (i > 0 && any_rescale) {
 #pragma unroll 1
           for (int blk = 0; blk < 4; ++blk) {
             const uint32_t taddr = tmem + lane_addr + kTmemO + blk * kRows + 32 * g_col;
@@ -765,15 +825,18 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
                                static_cast<uint64_t>(a.num_rows) * a.num_heads, 64, kRows,
                                CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != MLA_OK) return st;
-  const int box_rows = a.page_size < kTileTok ? a.page_size : kTileTok;  // one run of a tile
-  if (fp8)
-    st = make_tmap_2d(&tm_kv, a.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 576,
-                      static_cast<uint64_t>(a.num_cache_rows), 64, box_rows,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  // page size >= 64: a tile is 64 rows of one sub-page, loaded as one 3-D
+  // box of all nine chunks; smaller pages: one 2-D box per chunk and page.
+  const bool tile3d = a.page_size >= kTileTok;
+  const int box_rows = tile3d ? kTileTok : a.page_size;
+  const CUtensorMapDataType kv_type = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle kv_swz = fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  if (tile3d)
+    st = make_tmap_tile3d(&tm_kv, a.kv_cache, kv_type, fp8 ? 1 : 2, static_cast<uint64_t>(a.num_cache_rows),
+                          box_rows, kv_swz);
   else
-    st = make_tmap_2d(&tm_kv, a.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 576,
-                      static_cast<uint64_t>(a.num_cache_rows), 64, box_rows,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+    st = make_tmap_2d(&tm_kv, a.kv_cache, kv_type, fp8 ? 1 : 2, 576, static_cast<uint64_t>(a.num_cache_rows), 64,
+                      box_rows, kv_swz);
   if (st != MLA_OK) return st;
 
   int dev = 0;
@@ -823,6 +886,7 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
   p.max_qlen = a.max_qlen;
   p.num_rows = a.num_rows;
   p.max_len = a.subpage_stride * a.page_size;
+  p.tile3d = tile3d ? 1 : 0;
   const float kv_scale = fp8 ? a.kv_scale : 1.0f;
   p.score_scale_log2 = static_cast<float>(static_cast<double>(a.sm_scale) * kv_scale * 1.4426950408889634);
   p.out_scale = kv_scale;

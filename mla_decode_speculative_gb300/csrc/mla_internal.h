@@ -23,6 +23,11 @@ int *device_error_word();
 mla_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
                         int elem_bytes, uint64_t cols, uint64_t rows, uint32_t box_cols,
                         uint32_t box_rows, CUtensorMapSwizzle swizzle);
+// 3-D view of a [rows, 576] latent cache for whole-tile boxes (64 values x
+// box_rows x 9 chunks, chunk-major in shared memory).
+mla_status make_tmap_tile3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                            int elem_bytes, uint64_t rows, uint32_t box_rows,
+                            CUtensorMapSwizzle swizzle);
 
 // Launchers (arguments already validated on the host).
 struct TableLaunch {  // optional sub-page expansion (block_table == nullptr: none)

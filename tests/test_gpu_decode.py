@@ -131,6 +131,34 @@ def test_static_bound_does_not_change_results():
 
 # ------------------------------------------------------------------ full-size, sampled
 
+def test_repeated_steps_are_bit_identical():
+    """Each work item is computed start to finish by one CTA in a fixed
+    arithmetic order, whichever CTA claims it, so repeated steps must agree
+    bit for bit.  Many repetitions, some behind an L2 flush and some back to
+    back, shift the timing between the kernel's warp roles: a missing or
+    mis-phased barrier shows up as a mismatch here even when one run happens
+    to pass the oracle comparison."""
+    from mla_decode_speculative_gb300 import runner
+    for wl in (workloads.verify_mtp4_bf16(seed=4, batch=6, lo=64, hi=3000, num_segments=3),
+               workloads.fp8_mixed_qlen(seed=5, batch=5, lo=64, hi=2000, num_segments=2),
+               workloads.decode_qlen1_bf16()):
+        step = runner.step_for_workload(wl, "cuda")
+        q, kv, seq, ind, bt = runner.device_inputs(wl, "cuda")
+        flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+        first = None
+        for it in range(40):
+            if it % 3 == 0:
+                flush.fill_(float(it))
+            out, lse = step(q, kv, seq, ind, bt, wl.sm_scale, wl.kv_scale)
+            if first is None:
+                first = (out.clone(), lse.clone())
+                continue
+            assert torch.equal(out, first[0]) and torch.equal(lse, first[1]), f"{wl.name}: run {it} differs"
+        assert mla.get_device_error() == 0
+        ref_o, ref_l = oracle_reference(wl)
+        assert_close(first[0], first[1], ref_o, ref_l, wl.name)
+
+
 def test_verify_mtp4_full_size_sampled():
     _sampled_check(workloads.verify_mtp4_bf16(), 96, "verify qlen=4 batch 32 L 1k-8k S=16")
 
