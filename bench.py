@@ -77,7 +77,7 @@ def kv_bytes(wl) -> int:
 def decode_unit_bytes(wl) -> dict:
     """Algorithmic bytes of one launch of the decode kernel (unsharded):
     visible KV rows, the query rows, and the split-K partials it must write
-    (an (m, l) pair for every (row, head, segment), a 2 KiB float32 vector for
+    (an (m, l) pair for every (row, head, segment), a 1 KiB bf16 vector for
     every (row, head, segment) that holds a visible token)."""
     P = min(128, wl.block_size & -wl.block_size)
     S = wl.num_segments
@@ -91,7 +91,7 @@ def decode_unit_bytes(wl) -> dict:
     heads = wl.num_heads
     kv = kv_bytes(wl)
     q = wl.num_rows * heads * 1152
-    partial = (wl.num_rows * heads * S * 8 + active * heads * 2048) if S > 1 else \
+    partial = (wl.num_rows * heads * S * 8 + active * heads * 1024) if S > 1 else \
         wl.num_rows * heads * (1024 + 4)
     return {"kv": kv, "q": q, "partials": partial, "total": kv + q + partial}
 

@@ -170,7 +170,7 @@ typedef enum mla_decode_flags {
 
 /* Workspace bytes mla_decode_verify needs for `a`.  Layout, each region
  * starting on a 256-byte boundary, in this order:
- *   segm_out [T, H, S, 512] float32, segm_max [T, H, S], segm_sum [T, H, S]
+ *   segm_out [T, H, S, 512] bf16, segm_max [T, H, S] float32, segm_sum [T, H, S] float32
  *   (these three only when num_segments > 1), then 256 bytes of scheduler
  *   state (a work counter the call zeroes on the stream before its kernel).
  * Host only. */
@@ -213,10 +213,10 @@ typedef struct mla_merge_args {
   int num_rows;    /* T */
   int num_heads;   /* H */
   int num_parts;   /* S segments or W shards, 1 <= num_parts <= 1024 */
-  /* MLA_MERGE_SEGMENTS: [T, H, S, 512] float32 unnormalised partial outputs,
-   * [T, H, S] base-2 maxima and exp2 sums; a part with max = -inf is empty
-   * and its output is never read. */
-  const float *segm_out;
+  /* MLA_MERGE_SEGMENTS: [T, H, S, 512] bf16 unnormalised partial outputs
+   * (uint16 bit patterns), [T, H, S] float32 base-2 maxima and exp2 sums; a
+   * part with max = -inf is empty and its output is never read. */
+  const uint16_t *segm_out;
   const float *segm_max;
   const float *segm_sum;
   /* MLA_MERGE_STATES: [W, T, H, 512] bf16 outputs and [W, T, H] float32

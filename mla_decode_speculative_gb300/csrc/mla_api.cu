@@ -271,7 +271,7 @@ WorkspaceLayout decode_workspace_layout(const mla_decode_args &a) {
   if (a.num_segments > 1) {
     const size_t items = static_cast<size_t>(a.num_rows) * a.num_heads * a.num_segments;
     l.segm_out = off;
-    off += align256(items * 512 * sizeof(float));
+    off += align256(items * 512 * sizeof(uint16_t));
     l.segm_max = off;
     off += align256(items * sizeof(float));
     l.segm_sum = off;
@@ -463,7 +463,7 @@ mla_status mla_decode_verify(const mla_decode_args *a, void *workspace, size_t w
   d.sched = reinterpret_cast<int *>(w + lay.sched);
   const bool partials = a->num_segments > 1;
   if (partials) {
-    d.segm_out = reinterpret_cast<float *>(w + lay.segm_out);
+    d.segm_out = reinterpret_cast<uint16_t *>(w + lay.segm_out);
     d.segm_max = reinterpret_cast<float *>(w + lay.segm_max);
     d.segm_sum = reinterpret_cast<float *>(w + lay.segm_sum);
   }

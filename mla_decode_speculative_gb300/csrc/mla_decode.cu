@@ -90,7 +90,8 @@ struct Misc {
   uint64_t empty[kStages];
   uint64_t s_full[kStages];   // QK of the stage's tile retired
   uint64_t p_full[kStages];   // P^T of the stage's tile written
-  uint64_t q_full, q_empty, o_done, fin;
+  uint64_t o_done[kStages];   // PV of the stage's tile retired
+  uint64_t q_full, q_empty, fin;
   uint64_t work_full[kWorkRing], work_empty[kWorkRing];
   uint32_t tmem_base;
   int abort;
@@ -106,7 +107,7 @@ struct Params {
   const int32_t *qo_indptr;
   const int32_t *row_len;
   const int32_t *subpage_table;
-  float *segm_out;
+  __nv_bfloat16 *segm_out;  // unnormalised partial outputs, bf16
   float *segm_max;
   float *segm_sum;
   __nv_bfloat16 *out;
@@ -214,6 +215,25 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Half-warp transpose-reduce: lanes 16h .. 16h + 15 each hold 16 values
+// (column 16h + k in v[k]); on exit lane L holds the max (or sum) over its
+// half's 16 lanes of column L.
+template <bool kMax>
+__device__ __forceinline__ float half_reduce_scatter(float (&v)[16], int lane) {
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int k = 0; k < off; ++k) {
+      const float send = upper ? v[k] : v[k + off];
+      const float keep = upper ? v[k + off] : v[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+      v[k] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -270,10 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&misc.empty[i]), 1);
       mbar_init(smem_u32(&misc.s_full[i]), 1);
       mbar_init(smem_u32(&misc.p_full[i]), kNumSoftmaxWarps);
+      mbar_init(smem_u32(&misc.o_done[i]), 1);
     }
     mbar_init(smem_u32(&misc.q_full), 1);
     mbar_init(smem_u32(&misc.q_empty), 1);
-    mbar_init(smem_u32(&misc.o_done), 1);
     mbar_init(smem_u32(&misc.fin), 1);
     for (int i = 0; i < kWorkRing; ++i) {
       mbar_init(smem_u32(&misc.work_full[i]), 1);
@@ -483,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 1; kk < kTileTok / 16; ++kk)
               if (kk < n_k16) umma_bf16_ss_acc(t_o, da + kk * 128, dp + kk * 128, idesc_pv);
           }
+          umma_commit(smem_u32(&misc.o_done[st]));
           umma_commit(smem_u32(&misc.empty[st]));  // stage (V and P^T) free for the next load
-          umma_commit(smem_u32(&misc.o_done));
           ++gp;
         } else if (it_left == 0 && !no_more) {
           const uint32_t ws = k % kWorkRing;
@@ -553,8 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================================================== softmax warps
     const int g_col = warp >> 2;       // column group: rows 32g .. 32g+31 of the block
     const int wq = warp & 3;           // TMEM lane quarter
-    const bool s_lane = lane < 16;     // lanes 0-15 of a quarter hold S^T rows (M = 64)
-    const int tok = wq * 16 + (lane & 15);  // token row of S^T handled by this lane
+    // S^T (M = 64) puts token 16 q + i in TMEM lane 32 q + i: this thread
+    // handles token `tok` and the 16 columns 32g + 16h .. 32g + 16h + 15.
+    const int half = lane >> 4;
+    const int tok = wq * 16 + (lane & 15);
     const int dim_lane = wq * 32 + lane;    // dim row of an O^T block
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     const int my_col = 32 * g_col + lane;  // column whose statistics this lane keeps
@@ -594,11 +616,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&misc.work_empty[ws]));
         continue;
       }
-      const int *lens_g = &e.lens[32 * g_col];
-      float l_part[32];
-      float m_col[32];  // reference max of each of the group's columns (lane j keeps m_ref of column j)
+      const int *lens_h = &e.lens[32 * g_col + 16 * half];
+      float l_part[16];
+      float m_col[16];  // reference max of this thread's 16 columns (lane c keeps m_ref of group column c)
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < 16; ++j) {
         l_part[j] = 0.0f;
         m_col[j] = -INFINITY;
       }
@@ -646,16 +668,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         }
         tc_fence_after();
-        uint32_t sv[32];
-        tmem_ld32(tmem + lane_addr + kTmemS + st * 64 + 32 * g_col, sv);
+        uint32_t sv[16];
+        tmem_ld16x2(tmem + lane_addr + kTmemS + st * 64 + 32 * g_col, sv);
 
         // scaled scores (log2 units), causal + segment mask per column
-        float x[32];
+        float x[16];
         const int gtok = tok0 + tok;
-        const bool tok_in = s_lane && tok < n_valid;
+        const bool tok_in = tok < n_valid;
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const int4 lens = *reinterpret_cast<const int4 *>(&lens_g[4 * j4]);
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const int4 lens = *reinterpret_cast<const int4 *>(&lens_h[4 * j4]);
           const int lv[4] = {lens.x, lens.y, lens.z, lens.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -668,15 +690,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // first tile that sees data).  One barrier-reduction votes per group.
         bool exceed = false;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) exceed |= (x[j] - m_col[j] > kRescaleThreshold);
+        for (int j = 0; j < 16; ++j) exceed |= (x[j] - m_col[j] > kRescaleThreshold);
         const bool group_exceed = named_bar_red_or(1 + g_col, 128, exceed);
         bool any_rescale = false;
         float alpha = 1.0f;
         if (group_exceed) {
-          float red[32];
+          float red[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) red[j] = x[j];
-          const float wmax = warp_reduce_scatter<true>(red, lane);
+          for (int j = 0; j < 16; ++j) red[j] = x[j];
+          const float wmax = half_reduce_scatter<true>(red, lane);  // column `lane` of the group
           misc.red[red_buf][g_col][wq][lane] = wmax;
           named_bar_sync(1 + g_col, 128);
           const float tmax =
@@ -689,44 +711,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           any_rescale = __any_sync(0xffffffffu, alpha != 1.0f);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) m_col[j] = __shfl_sync(0xffffffffu, m_ref, j);
+          for (int j = 0; j < 16; ++j) m_col[j] = __shfl_sync(0xffffffffu, m_ref, 16 * half + j);
         }
 #pragma unroll
-        for (int j = 0; j < 32; ++j)  // probability (0 for masked entries and empty columns)
+        for (int j = 0; j < 16; ++j)  // probability (0 for masked entries and empty columns)
           x[j] = (x[j] == -INFINITY) ? 0.0f : fast_exp2(x[j] - m_col[j]);
         if (any_rescale) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) l_part[j] *= __shfl_sync(0xffffffffu, alpha, j);
+          for (int j = 0; j < 16; ++j) l_part[j] *= __shfl_sync(0xffffffffu, alpha, 16 * half + j);
         }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) l_part[j] += x[j];
+        for (int j = 0; j < 16; ++j) l_part[j] += x[j];
 
-        // P^T row `tok`, columns 32g .. 32g+31 (bf16, 128-byte swizzle), into
-        // the stage's rope chunk (the tile's QK has retired it).
+        // P^T row `tok`, columns 32g + 16h .. +15 (bf16, 128-byte swizzle),
+        // into the stage's rope chunk (the tile's QK has retired it).
         const uint32_t s_pt = s_stage + kPChunk * kChunkBytes;
-        if (s_lane) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t chunk = static_cast<uint32_t>((4 * g_col + q) ^ (tok & 7));
-            st_shared_v4(s_pt + tok * 128 + chunk * 16, pack_bf16(x[8 * q + 0], x[8 * q + 1]),
-                         pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
-                         pack_bf16(x[8 * q + 6], x[8 * q + 7]));
-          }
-          // V rows past the last valid token but inside the last 16-token MMA
-          // step hold stale or foreign data: zero them so 0 * V stays 0.
-          if (tok >= n_valid && tok < ((n_valid + 15) & ~15)) {
-            for (int c = 4 * g_col; c < 4 * g_col + 4; ++c)
-#pragma unroll
-              for (int c16 = 0; c16 < 8; ++c16)
-                st_shared_v4(s_stage + c * kChunkBytes + tok * 128 + c16 * 16, 0, 0, 0, 0);
-          }
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t chunk = static_cast<uint32_t>((4 * g_col + 2 * half + q) ^ (tok & 7));
+          st_shared_v4(s_pt + tok * 128 + chunk * 16, pack_bf16(x[8 * q + 0], x[8 * q + 1]),
+                       pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
+                       pack_bf16(x[8 * q + 6], x[8 * q + 7]));
         }
-        // PV of the previous tile must have retired before O is rescaled,
-        // and in any case before this tile's P^T is released: o_done is then
-        // observed phase by phase (a parity wait cannot tell phases two
-        // apart), and the epilogue's wait covers every PV of the item.
-        if (g > 0) {
-          if (ok && !mbar_wait(smem_u32(&misc.o_done), (g - 1) & 1u, abort_flag, budget)) {
+        // V rows past the last valid token but inside the last 16-token MMA
+        // step hold stale or foreign data: zero them so 0 * V stays 0 (this
+        // thread: two of the row's eight V chunks).
+        if (tok >= n_valid && tok < ((n_valid + 15) & ~15)) {
+          for (int c = 4 * g_col + 2 * half; c < 4 * g_col + 2 * half + 2; ++c)
+#pragma unroll
+            for (int c16 = 0; c16 < 8; ++c16)
+              st_shared_v4(s_stage + c * kChunkBytes + tok * 128 + c16 * 16, 0, 0, 0, 0);
+        }
+        // O is rescaled only after the previous tile's PV retired.  o_done
+        // has one barrier per stage, so a stage's completions are two tiles
+        // apart: the wait for tile g-1 can neither see a stale phase nor one
+        // two ahead (PV of tile g+1 needs this tile's P^T first).
+        if (i > 0 && any_rescale) {
+          if (ok && !mbar_wait(smem_u32(&misc.o_done[(g - 1) & 1u]), ((g - 1) >> 1) & 1u, abort_flag, budget)) {
             fail();
             ok = false;
           }
@@ -751,12 +772,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // ---- epilogue of the item: row sums, statistics, output
-      if (ok && !mbar_wait(smem_u32(&misc.o_done), (g - 1) & 1u, abort_flag, budget)) {
+      if (ok && !mbar_wait(smem_u32(&misc.o_done[(g - 1) & 1u]), ((g - 1) >> 1) & 1u, abort_flag, budget)) {
         fail();
         ok = false;
       }
       tc_fence_after();
-      const float wsum = warp_reduce_scatter<false>(l_part, lane);
+      const float wsum = half_reduce_scatter<false>(l_part, lane);  // column `lane` of the group
       misc.red[red_buf][g_col][wq][lane] = wsum;
       named_bar_sync(1 + g_col, 128);
       const float l_tot = misc.red[red_buf][g_col][0][lane] + misc.red[red_buf][g_col][1][lane] +
@@ -791,11 +812,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j)
             if (j < n_cols) o[static_cast<int64_t>(j) * 512] = __float2bfloat16_rn(__uint_as_float(ov[j]) * sc[j]);
         } else {
-          float *o = p.segm_out + (r0 * S + seg) * 512 + dim;
+          __nv_bfloat16 *o = p.segm_out + (r0 * S + seg) * 512 + dim;
           const int64_t stride = static_cast<int64_t>(S) * 512;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < n_cols && sc[j] != 0.0f) o[j * stride] = __uint_as_float(ov[j]) * sc[j];
+            if (j < n_cols && sc[j] != 0.0f) o[j * stride] = __float2bfloat16_rn(__uint_as_float(ov[j]) * sc[j]);
         }
       }
       tc_fence_before();  // O reads done before the next item's first PV overwrites O
@@ -863,7 +884,7 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
   p.qo_indptr = a.qo_indptr;
   p.row_len = a.row_len;
   p.subpage_table = a.subpage_table;
-  p.segm_out = d.segm_out;
+  p.segm_out = reinterpret_cast<__nv_bfloat16 *>(d.segm_out);
   p.segm_max = d.segm_max;
   p.segm_sum = d.segm_sum;
   p.out = static_cast<__nv_bfloat16 *>(a.out);

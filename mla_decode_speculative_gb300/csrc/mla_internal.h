@@ -46,7 +46,7 @@ mla_status launch_shard_rows(int num_reqs, int num_rows, const int32_t *qo_indpt
 
 struct DecodeLaunch {
   const mla_decode_args *a;
-  float *segm_out;
+  uint16_t *segm_out;  // bf16
   float *segm_max;
   float *segm_sum;
   int *sched;  // work-claim counter (workspace), zeroed before each launch
@@ -65,7 +65,7 @@ struct MergeLaunch {
   int num_rows;
   int num_heads;
   int num_parts;
-  const float *segm_out;
+  const uint16_t *segm_out;  // bf16
   const float *segm_max;
   const float *segm_sum;
   const void *part_out;

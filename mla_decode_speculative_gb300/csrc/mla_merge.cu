@@ -13,9 +13,11 @@
 // An empty part (max / lse = -inf) is never read; all parts empty gives
 // out = 0, lse = -inf.
 //
-// HBM-bound streaming reduction: one 128-thread block per (row, head); each
-// thread owns 4 of the 512 output dims, reads each live part with one
-// streaming load (8 parts in flight per thread) and writes 8 bytes of bf16.
+// Both modes read bf16 partial outputs (segment partials are stored in bf16
+// by the decode kernel).  HBM-bound streaming reduction: one 128-thread
+// block per (row, head); each thread owns 4 of the 512 output dims, reads
+// each live part with one 8-byte streaming load (8 parts in flight per
+// thread) and writes 8 bytes of bf16.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,7 +33,7 @@ constexpr int kThreadsPerItem = 128;  // 512 dims / 4 per thread
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct MergeParams {
-  const float *segm_out;
+  const __nv_bfloat16 *segm_out;
   const float *segm_max;
   const float *segm_sum;
   const __nv_bfloat16 *part_out;
@@ -61,14 +63,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // Loads this thread's 4 dims of part s of item it.
 template <bool kSeg>
 __device__ __forceinline__ float4 load4(const MergeParams &p, int64_t it, int s, int tid) {
-  if constexpr (kSeg) {
-    return __ldcs(reinterpret_cast<const float4 *>(p.segm_out + (it * p.num_parts + s) * 512) + tid);
-  } else {
-    const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(
-                               p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512) + tid);
-    return make_float4(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u),
-                       __uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
-  }
+  const __nv_bfloat16 *src = kSeg ? p.segm_out + (it * p.num_parts + s) * 512
+                                  : p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512;
+  const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(src) + tid);
+  return make_float4(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u),
+                     __uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
 }
 
 // Up to 32 parts: no block barrier.  Every thread reads the item's (tiny,
@@ -130,8 +129,8 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel_small(const Merg
 }
 
 // One 128-thread block per (row, head): thread t owns output dims 4t..4t+3,
-// so every live part costs each thread one 16-byte (f32) or 8-byte (bf16)
-// load, and up to 8 parts are in flight per thread.
+// so every live part costs each thread one 8-byte load, and up to 8 parts
+// are in flight per thread.
 template <bool kSeg>
 __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel(const MergeParams p) {
   __shared__ float s_w[kMaxParts];
@@ -214,17 +213,13 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel(const MergeParam
       const int k = min(k0 + u, n_live - 1);  // padding re-reads the last live part, weight 0
       const int s = s_idx[k];
       wv[u] = (k0 + u < n_live) ? s_w[k] : 0.0f;
-      if constexpr (kSeg) {
-        const float4 x = __ldcs(reinterpret_cast<const float4 *>(p.segm_out + (it * n + s) * 512) + tid);
-        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-      } else {
-        const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(
-                                   p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512) + tid);
-        v[u][0] = __uint_as_float(x.x << 16);
-        v[u][1] = __uint_as_float(x.x & 0xffff0000u);
-        v[u][2] = __uint_as_float(x.y << 16);
-        v[u][3] = __uint_as_float(x.y & 0xffff0000u);
-      }
+      const __nv_bfloat16 *src = kSeg ? p.segm_out + (it * n + s) * 512
+                                      : p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512;
+      const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(src) + tid);
+      v[u][0] = __uint_as_float(x.x << 16);
+      v[u][1] = __uint_as_float(x.x & 0xffff0000u);
+      v[u][2] = __uint_as_float(x.y << 16);
+      v[u][3] = __uint_as_float(x.y & 0xffff0000u);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
@@ -240,7 +235,7 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel(const MergeParam
 
 mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
   MergeParams p{};
-  p.segm_out = m.segm_out;
+  p.segm_out = reinterpret_cast<const __nv_bfloat16 *>(m.segm_out);
   p.segm_max = m.segm_max;
   p.segm_sum = m.segm_sum;
   p.part_out = static_cast<const __nv_bfloat16 *>(m.part_out);

@@ -244,6 +244,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "r"(taddr)
       : "memory");
 }
+// 16 TMEM lanes x 2 column halves: threads 0-15 read lanes base+0..15 at
+// columns col..col+15, threads 16-31 the same lanes at columns
+// col+16..col+31 (the second half is the immediate split offset), so a
+// warp reads a 16-lane region with every thread holding 16 values.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 16;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : MLA_R8(0), MLA_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
 #undef MLA_R8
 #define MLA_W8(o) "r"(v[o + 0]), "r"(v[o + 1]), "r"(v[o + 2]), "r"(v[o + 3]), \
                   "r"(v[o + 4]), "r"(v[o + 5]), "r"(v[o + 6]), "r"(v[o + 7])

@@ -281,9 +281,9 @@ def workspace_views(workspace: torch.Tensor, num_rows: int, num_heads: int, num_
     """The documented workspace layout: (segm_out [T,H,S,512], segm_max [T,H,S], segm_sum [T,H,S])."""
     items = num_rows * num_heads * num_segments
     a256 = lambda x: (x + 255) & ~255
-    o_bytes = a256(items * 512 * 4)
+    o_bytes = a256(items * 512 * 2)
     m_bytes = a256(items * 4)
-    segm_out = workspace[:items * 512 * 4].view(torch.float32).view(num_rows, num_heads, num_segments, 512)
+    segm_out = workspace[:items * 512 * 2].view(torch.bfloat16).view(num_rows, num_heads, num_segments, 512)
     segm_max = workspace[o_bytes:o_bytes + items * 4].view(torch.float32).view(num_rows, num_heads, num_segments)
     segm_sum = workspace[o_bytes + m_bytes:o_bytes + m_bytes + items * 4].view(torch.float32).view(
         num_rows, num_heads, num_segments)
@@ -291,7 +291,7 @@ def workspace_views(workspace: torch.Tensor, num_rows: int, num_heads: int, num_
 
 
 def merge_segments(segm_out, segm_max, segm_sum, out=None, lse=None, stream=None):
-    """mla_merge_segments, segment mode: [T,H,S,512] f32 + [T,H,S] base-2 stats."""
+    """mla_merge_segments, segment mode: [T,H,S,512] bf16 + [T,H,S] f32 base-2 stats."""
     T, H, S, dv = segm_out.shape
     if out is None:
         out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=segm_out.device)
@@ -299,7 +299,7 @@ def merge_segments(segm_out, segm_max, segm_sum, out=None, lse=None, stream=None
         lse = torch.empty((T, H), dtype=torch.float32, device=segm_out.device)
     m = MergeArgs()
     m.mode, m.num_rows, m.num_heads, m.num_parts = MLA_MERGE_SEGMENTS, T, H, S
-    m.segm_out = _ptr(segm_out, torch.float32, "segm_out")
+    m.segm_out = _ptr(segm_out, torch.bfloat16, "segm_out")
     m.segm_max = _ptr(segm_max, torch.float32, "segm_max")
     m.segm_sum = _ptr(segm_sum, torch.float32, "segm_sum")
     m.out = _ptr(out, torch.bfloat16, "out")

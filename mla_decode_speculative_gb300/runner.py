@@ -48,7 +48,7 @@ class VerifyStep:
         ws = 256  # scheduler state
         if num_segments > 1:
             items = num_rows * num_heads * num_segments
-            ws += ((items * 512 * 4 + 255) & ~255) + 2 * ((items * 4 + 255) & ~255)
+            ws += ((items * 512 * 2 + 255) & ~255) + 2 * ((items * 4 + 255) & ~255)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
 
     def __call__(self, q: torch.Tensor, kv_cache: torch.Tensor, seq_lens: torch.Tensor,

@@ -199,9 +199,11 @@ def verify_mtp4_bf16(seed: int = 0, batch: int = 32, lo: int = 1024, hi: int = 8
 
 
 def fp8_mixed_qlen(seed: int = 0, batch: int = 64, lo: int = 512, hi: int = 32768,
-                   num_segments: int = 4, device=None) -> Workload:
+                   num_segments: int = 16, device=None) -> Workload:
     """fp8_e4m3 cache: batch 64, 12 heads, qlen U{1,2,3}, seq_len log-uniform
-    [512, 32k], block 64."""
+    [512, 32k], block 64.  16 split-K segments: the longest request then
+    splits into items of <= 2048 tokens, below the per-SM share of the batch
+    (~3.3k tokens on 152 SMs), so no single item sets the step time."""
     g = _gen(seed + 2000)
     u = torch.rand(batch, generator=g, dtype=torch.float64).numpy()
     L = np.floor(np.exp(np.log(lo) + u * (np.log(hi) - np.log(lo)))).astype(np.int32)
@@ -212,9 +214,10 @@ def fp8_mixed_qlen(seed: int = 0, batch: int = 64, lo: int = 512, hi: int = 3276
 
 
 def dcp8_verify_bf16(seed: int = 0, batch: int = 16, context: int = 131072,
-                     world_size: int = 8, num_segments: int = 8, device=None) -> Workload:
+                     world_size: int = 8, num_segments: int = 19, device=None) -> Workload:
     """Simulated 8-way round-robin context-sharded verify: batch 16, 16 heads,
-    qlen 4, context 128k, bf16, block 64."""
+    qlen 4, context 128k, bf16, block 64.  19 split-K segments per shard:
+    16 x 19 = 304 work items per shard pass, two per SM on 152 SMs."""
     return make_workload(f"dcp{world_size}_verify_bf16_b{batch}_h16_qlen4_L{context}_bs64_s{num_segments}",
                          [context] * batch, [4] * batch, 16, 64, "bf16", world_size,
                          num_segments, seed, device=device,

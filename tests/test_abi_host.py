@@ -87,6 +87,6 @@ def test_workspace_size_formula(L):
     a.num_rows, a.num_heads, a.num_segments = 128, 16, 16
     items = 128 * 16 * 16
     r256 = lambda x: (x + 255) // 256 * 256
-    assert L.mla_decode_verify_workspace(ctypes.byref(a)) == r256(items * 2048) + 2 * r256(items * 4) + 256
+    assert L.mla_decode_verify_workspace(ctypes.byref(a)) == r256(items * 1024) + 2 * r256(items * 4) + 256
     a.num_segments = 1
     assert L.mla_decode_verify_workspace(ctypes.byref(a)) == 256

@@ -107,7 +107,7 @@ def test_segment_partials_match_oracle():
                                           wl.sm_scale, wl.block_tables[0], wl.block_size, 5,
                                           oracle.page_size(wl.block_size))
     gm, gs = segm_max.cpu().numpy(), segm_sum.cpu().numpy()
-    go = segm_out.cpu().numpy()
+    go = segm_out.float().cpu().numpy()  # bf16 partial outputs
     live = sm > 0
     assert (np.isneginf(gm) == ~live).all(), "GPU and oracle disagree on which segments are empty"
     # normalised segment output and segment LSE (invariant to the reference max)

@@ -25,9 +25,11 @@ def test_merge_segments_matches_oracle(T, H, S):
         m[0, 0, :] = -np.inf  # a fully empty item
         l[0, 0, :] = 0
         acc[0, 0, :] = np.nan
-    out, lse = mla.merge_segments(torch.tensor(acc, device="cuda"), torch.tensor(m, device="cuda"),
+    # segment partial outputs are bf16; the oracle merges the same rounded values
+    acc_bf = torch.tensor(acc).to(torch.bfloat16)
+    out, lse = mla.merge_segments(acc_bf.to("cuda"), torch.tensor(m, device="cuda"),
                                   torch.tensor(l, device="cuda"))
-    ref_o, ref_l = oracle.merge_segments(np.nan_to_num(acc, nan=0.0).astype(np.float64),
+    ref_o, ref_l = oracle.merge_segments(np.nan_to_num(acc_bf.float().numpy(), nan=0.0).astype(np.float64),
                                          m.astype(np.float64), l.astype(np.float64))
     assert_close(out, lse, ref_o, ref_l, "segment merge")
     if S > 1:
