@@ -65,6 +65,12 @@ def _load():
             lib.oracle_plan_rows.restype = c_int
             lib.oracle_rr_local_len.argtypes = [c_i64, c_int, c_int]
             lib.oracle_rr_local_len.restype = c_i64
+            lib.oracle_il_local_len.argtypes = [c_i64, c_int, c_int, c_int]
+            lib.oracle_il_local_len.restype = c_i64
+            lib.oracle_il_owner.argtypes = [c_i64, c_int, c_int]
+            lib.oracle_il_owner.restype = c_int
+            lib.oracle_il_local_index.argtypes = [c_i64, c_int, c_int]
+            lib.oracle_il_local_index.restype = c_i64
             lib.oracle_shard_row_view.argtypes = [c_int, i32p, c_int, c_int, c_int, i32p]
             lib.oracle_shard_row_view.restype = c_int
             lib.oracle_subpage_table.argtypes = [c_int, i32p, i32p, c_int, c_int, c_int, i32p, c_int]
@@ -85,7 +91,7 @@ def _load():
             lib.oracle_merge_states.restype = None
             lib.oracle_e4m3_encode_rne_sat.argtypes = [ctypes.c_float]
             lib.oracle_e4m3_encode_rne_sat.restype = ctypes.c_uint8
-            lib.oracle_write_kv.argtypes = [c_int, i32p, i32p, vp, c_int, c_int, i32p, c_int, c_int,
+            lib.oracle_write_kv.argtypes = [c_int, i32p, i32p, vp, c_int, c_int, c_int, i32p, c_int, c_int,
                                             vp, c_int, ctypes.c_float, c_i64]
             lib.oracle_write_kv.restype = c_int
             _lib = lib
@@ -143,9 +149,25 @@ def rr_local_len(w: int, world_size: int, rank: int) -> int:
     return int(_load().oracle_rr_local_len(int(w), int(world_size), int(rank)))
 
 
+def il_local_len(w: int, world_size: int, rank: int, interleave: int) -> int:
+    """Positions g < w that rank r holds under round-robin with interleave I
+    (runs of I positions dealt in turn; the pages support only I = 1)."""
+    return int(_load().oracle_il_local_len(int(w), int(world_size), int(rank), int(interleave)))
+
+
+def il_owner(g: int, world_size: int, interleave: int) -> int:
+    """Rank holding global position g: (g div I) mod W."""
+    return int(_load().oracle_il_owner(int(g), int(world_size), int(interleave)))
+
+
+def il_local_index(g: int, world_size: int, interleave: int) -> int:
+    """Local index of global position g on its rank: (g div (I*W)) * I + g mod I."""
+    return int(_load().oracle_il_local_index(int(g), int(world_size), int(interleave)))
+
+
 def shard_row_view(row_len_global, world_size, rank, interleave=1):
     """Per-row shard-local lengths counted from each row's global window
-    [vLLM #51705, 实现拆解 2]; interleave != 1 raises (unsupported)."""
+    [vLLM #51705, 实现拆解 2]; interleave I >= 1 (I = 1 is the pages' form)."""
     g, gp = _i32(row_len_global)
     out = np.zeros_like(g)
     _, op = _i32(out)
@@ -292,7 +314,7 @@ def merge_states(out_parts, lse_parts):
 
 
 def sharded_attention(qo_indptr, row_len_global, q_bits, kv, kv_scale, sm_scale,
-                      shard_block_tables, block_size, world_size, sel=None):
+                      shard_block_tables, block_size, world_size, sel=None, interleave=1):
     """DCP verify as the pages describe it: every shard r attends the tokens
     it holds within each row's global window (counted by the shard row view),
     reading its own block table; the W partial states are merged in the
@@ -300,7 +322,7 @@ def sharded_attention(qo_indptr, row_len_global, q_bits, kv, kv_scale, sm_scale,
     cache ``kv``.  Returns (out, lse, per-shard (out_r, lse_r) lists)."""
     parts_out, parts_lse = [], []
     for r in range(world_size):
-        local = shard_row_view(row_len_global, world_size, r)
+        local = shard_row_view(row_len_global, world_size, r, interleave)
         o, l = attention(qo_indptr, local, q_bits, kv, kv_scale, sm_scale,
                          shard_block_tables[r], block_size, sel=sel)
         parts_out.append(o)
@@ -315,7 +337,7 @@ def e4m3_encode(x: float) -> int:
 
 
 def write_kv(seq_lens, qo_indptr, kv_new_bits, world_size, rank, block_table, block_size,
-             cache, kv_scale=1.0):
+             cache, kv_scale=1.0, interleave=1):
     """Owner-filtered paged write of the new verify tokens into one rank's cache
     [sglang #34432, 实现拆解 4, set_mla_kv_buffer].  cache (uint16 bf16 bits or
     uint8 e4m3 codes, [rows, 576]) is updated in place."""
@@ -326,6 +348,6 @@ def write_kv(seq_lens, qo_indptr, kv_new_bits, world_size, rank, block_table, bl
     assert cache.flags["C_CONTIGUOUS"] and cache.shape[1] == D_K
     dt = 0 if cache.dtype == np.uint16 else 1
     _check(_load().oracle_write_kv(seq.shape[0], sp, ip, kvn.ctypes.data, int(world_size), int(rank),
-                                   bp, bt.shape[1], int(block_size), cache.ctypes.data, dt,
+                                   int(interleave), bp, bt.shape[1], int(block_size), cache.ctypes.data, dt,
                                    float(kv_scale), cache.shape[0]), "write_kv")
     return cache

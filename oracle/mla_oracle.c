@@ -104,18 +104,42 @@ int64_t oracle_rr_local_len(int64_t w, int world_size, int rank) {
   return top / world_size + 1; /* top >= 0, so C division is floor */
 }
 
+/* Round-robin with interleave I (the pages support only I = 1 and reject
+ * the rest as unverified [vLLM #51705, 实现拆解 1]; the reading used here is
+ * the plain generalisation of g(j) = j*W + r): the global positions are cut
+ * into runs of I consecutive positions, dealt to the ranks in turn, so
+ * position g belongs to rank (g div I) mod W, at local index
+ * (g div (I*W)) * I + g mod I.  For a window of w positions, rank r holds
+ * I per full cycle of I*W positions plus its part of the last, partial
+ * cycle.  I = 1 reduces to oracle_rr_local_len.                              */
+int64_t oracle_il_local_len(int64_t w, int world_size, int rank, int interleave) {
+  if (w <= 0) return 0;
+  const int64_t cycle = (int64_t)interleave * world_size;
+  int64_t rem = w % cycle - (int64_t)rank * interleave;
+  if (rem < 0) rem = 0;
+  if (rem > interleave) rem = interleave;
+  return (w / cycle) * interleave + rem;
+}
+int oracle_il_owner(int64_t g, int world_size, int interleave) {
+  return (int)((g / interleave) % world_size);
+}
+int64_t oracle_il_local_index(int64_t g, int world_size, int interleave) {
+  return (g / ((int64_t)interleave * world_size)) * interleave + g % interleave;
+}
+
 /* Shard row view: each verify row keeps its own shard-local length, counted
  * from the row's GLOBAL window (never "local length minus an offset").
- * [vLLM #51705, 实现拆解 2].  interleave other than 1 is rejected
- * [vLLM #51705, 实现拆解 1, _segmented_dcp_verify_supported].               */
+ * [vLLM #51705, 实现拆解 2].  interleave 1 is the pages' form; other values
+ * follow the generalisation above.                                          */
 int oracle_shard_row_view(int num_rows, const int32_t *row_len_global,
                           int world_size, int rank, int interleave,
                           int32_t *row_len_local) {
-  if (interleave != 1) return ORC_ERR_UNSUPPORTED;
+  if (interleave < 1) return ORC_ERR_UNSUPPORTED;
   if (world_size < 1 || rank < 0 || rank >= world_size) return ORC_ERR_ARG;
   for (int i = 0; i < num_rows; i++)
-    row_len_local[i] =
-        (int32_t)oracle_rr_local_len(row_len_global[i], world_size, rank);
+    row_len_local[i] = interleave == 1
+                           ? (int32_t)oracle_rr_local_len(row_len_global[i], world_size, rank)
+                           : (int32_t)oracle_il_local_len(row_len_global[i], world_size, rank, interleave);
   return ORC_OK;
 }
 
@@ -483,24 +507,26 @@ uint8_t oracle_e4m3_encode_rne_sat(float xf) {
  * filtering by owner and dividing by the shard count; key snippet
  * g(j) = j * W + r].  Request b's qlen_b new tokens sit at global positions
  * g = L_b - qlen_b + t (t < qlen_b; row qo_indptr[b] + t of kv_new).  Rank
- * `rank` of W keeps the tokens with g mod W == rank, at its local index
- * j = g div W, i.e. cache row block_table[b][j / block_size] * block_size +
+ * `rank` of W keeps the tokens it owns (g mod W == rank for interleave 1; the
+ * generalisation above otherwise), at its local index j (g div W for
+ * interleave 1), i.e. cache row block_table[b][j / block_size] * block_size +
  * j % block_size.  bf16 caches receive the row's 576 bf16 values unchanged;
  * fp8 caches receive e4m3 codes of (value / kv_scale) computed in float32
  * (round to nearest even, saturating).  Returns 0 or an error code.          */
 int oracle_write_kv(int num_reqs, const int32_t *seq_lens, const int32_t *qo_indptr,
-                    const uint16_t *kv_new, int world_size, int rank,
+                    const uint16_t *kv_new, int world_size, int rank, int interleave,
                     const int32_t *block_table, int bt_stride, int block_size, void *cache,
                     int kv_dtype, float kv_scale, int64_t cache_rows) {
-  if (world_size < 1 || rank < 0 || rank >= world_size || block_size < 1) return ORC_ERR_ARG;
+  if (world_size < 1 || rank < 0 || rank >= world_size || block_size < 1 || interleave < 1)
+    return ORC_ERR_ARG;
   for (int b = 0; b < num_reqs; b++) {
     int qlen = qo_indptr[b + 1] - qo_indptr[b];
     int L = seq_lens[b];
     if (qlen < 1 || qlen > L) return ORC_ERR_QLEN;
     for (int t = 0; t < qlen; t++) {
       int64_t g = (int64_t)L - qlen + t;
-      if (g % world_size != rank) continue;
-      int64_t j = g / world_size;
+      if (oracle_il_owner(g, world_size, interleave) != rank) continue;
+      int64_t j = oracle_il_local_index(g, world_size, interleave);
       int32_t blk = block_table[(int64_t)b * bt_stride + j / block_size];
       int64_t slot = (int64_t)blk * block_size + j % block_size;
       if (blk < 0 || slot >= cache_rows) return ORC_ERR_SLOT;

@@ -108,11 +108,59 @@ def test_negative_control_subtraction_breaks_the_sum():
     assert bad == ql - 1      # every row but the last is wrong
 
 
-def test_shard_row_view_rejects_interleave():
+def test_shard_row_view_rejects_bad_interleave_and_rank():
     with pytest.raises(oracle.OracleError):
-        oracle.shard_row_view([10, 11], 4, 0, interleave=2)
+        oracle.shard_row_view([10, 11], 4, 0, interleave=0)
     with pytest.raises(oracle.OracleError):
         oracle.shard_row_view([10], 4, 4)
+
+
+# --------------------------------------------------------------------------- interleave > 1
+# Runs of I consecutive positions are dealt to the ranks in turn (I = 1 is the
+# pages' g(j) = j * W + r).  Pinned by enumeration, not by the closed forms.
+
+def _deal(w, W, I):
+    """Enumerate positions 0 .. w-1 run by run: per rank, its positions in order."""
+    held = [[] for _ in range(W)]
+    for run_start in range(0, w, I):
+        held[(run_start // I) % W].extend(range(run_start, min(run_start + I, w)))
+    return held
+
+
+def test_interleave_counts_brute_force():
+    for W in range(1, 7):
+        for I in range(1, 6):
+            for w in range(0, 140):
+                held = _deal(w, W, I)
+                counts = [oracle.il_local_len(w, W, r, I) for r in range(W)]
+                assert counts == [len(h) for h in held], (w, W, I)
+                assert sum(counts) == w
+                if I == 1:
+                    assert counts == [oracle.rr_local_len(w, W, r) for r in range(W)]
+
+
+def test_interleave_owner_and_local_index_enumerated():
+    # each rank's positions, in increasing order, sit at local indices 0, 1, 2, ...
+    # (so every row's shard window is a prefix of the shard's local sequence)
+    for W in (1, 2, 3, 8):
+        for I in (1, 2, 4, 16):
+            held = _deal(300, W, I)
+            for r in range(W):
+                for j, g in enumerate(held[r]):
+                    assert oracle.il_owner(g, W, I) == r
+                    assert oracle.il_local_index(g, W, I) == j
+
+
+def test_interleave_row_view_per_row_causality():
+    for W, I in ((2, 2), (3, 4), (8, 16), (4, 1)):
+        for L, ql in ((50, 4), (17, 8), (1000, 3), (64, 64)):
+            row_len, _, _ = oracle.plan_rows([L], [0, ql])
+            views = np.stack([oracle.shard_row_view(row_len, W, r, I) for r in range(W)])
+            assert (views.sum(axis=0) == row_len).all()
+            for t in range(ql - 1):
+                gain = views[:, t + 1] - views[:, t]
+                assert set(gain.tolist()) <= {0, 1} and gain.sum() == 1
+                assert gain[oracle.il_owner(int(row_len[t]), W, I)] == 1
 
 
 def test_subpage_golden():
@@ -359,11 +407,13 @@ def test_merge_identity_and_arbitrary_split():
     assert (o4 == 0).all() and np.isneginf(l4).all()
 
 
-def _shard_layout(dense, W, bs, rng):
-    """Round-robin layout built by enumeration: global position g of request b
-    goes to shard g % W at local index g // W.  Returns per-shard block tables
-    over one shared pool."""
-    shard_dense = [[d[r::W] for d in dense] for r in range(W)]
+def _shard_layout(dense, W, bs, rng, I=1):
+    """Round-robin layout built by enumeration: runs of I positions of request b
+    dealt to the shards in turn, each shard keeping its positions in order (for
+    I = 1: position g at shard g % W, local index g // W).  Returns per-shard
+    block tables over one shared pool."""
+    shard_dense = [[d[np.array(_deal(d.shape[0], W, I)[r], dtype=np.int64)] for d in dense]
+                   for r in range(W)]
     pools, tables = [], []
     offset = 0
     for r in range(W):
@@ -377,6 +427,23 @@ def _shard_layout(dense, W, bs, rng):
     mb = max(t.shape[1] for t in tables)
     tables = [np.pad(t, ((0, 0), (0, mb - t.shape[1])), constant_values=-1) for t in tables]
     return np.concatenate(pools), np.stack(tables)
+
+
+@pytest.mark.parametrize("W,I", [(3, 2), (8, 4), (2, 16)])
+def test_sharded_merge_equals_unsharded_interleaved(W, I):
+    rng = np.random.default_rng(60 + W)
+    seq, ql, H, bs = [37, 5, 64], [4, 3, 2], 2, 4
+    dense = [f32_to_bf16_bits(rng.standard_normal((L, D_K))) for L in seq]
+    q = f32_to_bf16_bits(rng.standard_normal((sum(ql), H, D_K)))
+    ind = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    row_len, _, _ = oracle.plan_rows(seq, ind)
+    pool, bt = paged_from_dense(dense, bs, rng)
+    ref_out, ref_lse = oracle.attention(ind, row_len, q, pool, 1.0, SM, bt, bs)
+    spool, sbt = _shard_layout(dense, W, bs, rng, I)
+    out, lse, _, _ = oracle.sharded_attention(ind, row_len, q, spool, 1.0, SM, sbt, bs, W,
+                                              interleave=I)
+    np.testing.assert_allclose(out, ref_out, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
 
 
 @pytest.mark.parametrize("W", [2, 3, 8])
@@ -432,15 +499,15 @@ def test_e4m3_encode_ties_saturation_and_sign():
     assert oracle.e4m3_encode(float("nan")) == 0x7F
 
 
-@pytest.mark.parametrize("W", [1, 3, 8])
-def test_write_kv_places_tokens_by_round_robin(W):
-    rng = np.random.default_rng(40 + W)
+@pytest.mark.parametrize("W,I", [(1, 1), (3, 1), (8, 1), (3, 2), (8, 4)])
+def test_write_kv_places_tokens_by_round_robin(W, I):
+    rng = np.random.default_rng(40 + W + 7 * I)
     seq, ql, bs = [37, 5, 64, 9], [4, 2, 3, 1], 8
     B = len(seq)
     T = sum(ql)
     ind = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
     kv_new = f32_to_bf16_bits(rng.standard_normal((T, D_K)))
-    cap = [-(-L // W) for L in seq]
+    cap = [max(1, max(len(h) for h in _deal(L, W, I))) for L in seq]
     nb = [-(-c // bs) for c in cap]
     for r in range(W):
         perm = rng.permutation(sum(nb) + 2).astype(np.int32)
@@ -450,14 +517,16 @@ def test_write_kv_places_tokens_by_round_robin(W):
             bt[b, :nb[b]] = perm[pos:pos + nb[b]]
             pos += nb[b]
         cache = np.zeros(((sum(nb) + 2) * bs, D_K), np.uint16)
-        oracle.write_kv(seq, ind, kv_new, W, r, bt, bs, cache)
-        # expected, by enumerating positions: token t of b at g = L - qlen + t
+        oracle.write_kv(seq, ind, kv_new, W, r, bt, bs, cache, interleave=I)
+        # expected, by enumerating positions: token t of b at g = L - qlen + t,
+        # at the rank's local index = its rank among the positions that rank holds
         want = np.zeros_like(cache)
         for b in range(B):
+            held = _deal(seq[b], W, I)[r]
             for t in range(ql[b]):
                 g = seq[b] - ql[b] + t
-                if g % W == r:
-                    j = g // W
+                if g in held:
+                    j = held.index(g)
                     want[bt[b, j // bs] * bs + j % bs] = kv_new[ind[b] + t]
         assert (cache == want).all()
 
