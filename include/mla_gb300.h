@@ -52,12 +52,12 @@ typedef struct CUstream_st *mla_stream_t;
 
 #define MLA_D_QK 576  /* q / K width: 512 latent + 64 rope   */
 #define MLA_D_V 512   /* V / output width: the 512-d latent */
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 
 typedef enum mla_status {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,  /* a size, pointer or stride the host can see is wrong */
-  MLA_ERR_UNSUPPORTED = 2,  /* valid but not supported: interleave != 1, page size < 8, ... */
+  MLA_ERR_UNSUPPORTED = 2,  /* valid but not supported: page size < 8, unknown dtype, ... */
   MLA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than mla_decode_verify_workspace() */
   MLA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed; see mla_last_error_string() */
   MLA_ERR_DEVICE_CHECK = 5  /* returned by mla_get_device_error when a device check fired */
@@ -120,9 +120,13 @@ mla_status mla_plan_rows(int num_reqs, int num_rows, const int32_t *seq_lens,
  * positions sees
  *     row_len_local = floor((w - 1 - rank) / W) + 1  if w - 1 - rank >= 0, else 0
  * tokens of this rank -- counted from the row's own global window, never as
- * "request's local length minus the causal offset".  Only interleave == 1 is
- * supported [vLLM #51705, 实现拆解 1, _segmented_dcp_verify_supported]; any
- * other value returns MLA_ERR_UNSUPPORTED.
+ * "request's local length minus the causal offset".  interleave I > 1 goes
+ * beyond the pages, which accept only I = 1 [vLLM #51705, 实现拆解 1,
+ * _segmented_dcp_verify_supported]: runs of I consecutive positions are
+ * dealt to the ranks in turn, position g on rank (g div I) mod W at local
+ * index (g div (I*W)) * I + g mod I, and the rank sees
+ *     row_len_local = (w div (I*W)) * I + clamp(w mod (I*W) - rank * I, 0, I).
+ * interleave < 1 returns MLA_ERR_INVALID_ARG.
  * Optionally (block_table != NULL, the SHARD's own physical block table over
  * its local tokens) it writes the shard's sub-page table exactly as
  * mla_plan_rows does, sized by the request's longest shard-local row; the
@@ -170,7 +174,11 @@ typedef enum mla_decode_flags {
 
 /* Workspace bytes mla_decode_verify needs for `a`.  Layout, each region
  * starting on a 256-byte boundary, in this order:
- *   segm_out [T, H, S, 512] bf16, segm_max [T, H, S] float32, segm_sum [T, H, S] float32
+ *   segm_out [B, RB, S, 512, 64] bf16: RB = ceil(max_qlen * H / 64) row blocks
+ *     per request; block (b, rb, s) holds, dim-major (64 rows innermost),
+ *     segment s of request b's rows rb*64 .. rb*64 + 63, a request's rows
+ *     numbered t * H + h; rows past the request's qlen * H are unused;
+ *   segm_max [T, H, S] float32, segm_sum [T, H, S] float32
  *   (these three only when num_segments > 1), then 256 bytes of scheduler
  *   state (a work counter the call zeroes on the stream before its kernel).
  * Host only. */
@@ -213,12 +221,17 @@ typedef struct mla_merge_args {
   int num_rows;    /* T */
   int num_heads;   /* H */
   int num_parts;   /* S segments or W shards, 1 <= num_parts <= 1024 */
-  /* MLA_MERGE_SEGMENTS: [T, H, S, 512] bf16 unnormalised partial outputs
-   * (uint16 bit patterns), [T, H, S] float32 base-2 maxima and exp2 sums; a
-   * part with max = -inf is empty and its output is never read. */
+  /* MLA_MERGE_SEGMENTS: the decode workspace's partials: segm_out
+   * [B, RB, S, 512, 64] bf16 unnormalised outputs (uint16 bit patterns; the
+   * block layout of mla_decode_verify_workspace), segm_max / segm_sum
+   * [T, H, S] float32 base-2 maxima and exp2 sums.  A part with max = -inf
+   * is empty and contributes nothing (its output is not read as a value). */
   const uint16_t *segm_out;
   const float *segm_max;
   const float *segm_sum;
+  const int32_t *qo_indptr;  /* segment mode: [B + 1] device, as for mla_decode_verify */
+  int num_reqs;              /* segment mode: B */
+  int max_qlen;              /* segment mode: bound on qlen_b, fixes RB */
   /* MLA_MERGE_STATES: [W, T, H, 512] bf16 outputs and [W, T, H] float32
    * natural-log LSEs; a part with lse = -inf is empty and never read. */
   const void *part_out;
@@ -250,7 +263,9 @@ mla_status mla_merge_segments(const mla_merge_args *a, mla_stream_t stream);
  * is the plain (unsharded) write.  bf16 caches receive the values unchanged;
  * fp8 caches (kv_dtype = MLA_KV_FP8_E4M3) receive the e4m3 codes of
  * value / kv_scale computed in float32, rounded to nearest even and
- * saturated to +-448.  Only interleave 1 is supported.
+ * saturated to +-448.  interleave I > 1 places position g on rank
+ * (g div I) mod W at local index (g div (I*W)) * I + g mod I, as
+ * mla_shard_row_view counts it.
  * Device checks: MLA_DEV_BAD_INDPTR, MLA_DEV_BAD_QLEN, MLA_DEV_BAD_BLOCK_ID
  * (the token is then not written). */
 mla_status mla_write_kv(int num_reqs, int num_rows, const int32_t *seq_lens,

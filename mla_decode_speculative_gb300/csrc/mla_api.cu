@@ -30,6 +30,17 @@ __device__ __forceinline__ int rr_count(int w, int W, int r) {
   const int top = w - 1 - r;
   return top >= 0 ? top / W + 1 : 0;
 }
+// Interleave I > 1 (runs of I consecutive positions dealt to the ranks in
+// turn; the pages stop at I = 1): I positions per full cycle of I * W plus
+// the rank's part of the last, partial cycle.
+__device__ __forceinline__ int il_count(int w, int W, int r, int I) {
+  if (I == 1) return rr_count(w, W, r);
+  if (w <= 0) return 0;
+  const int64_t cycle = static_cast<int64_t>(I) * W;
+  int64_t rem = w % cycle - static_cast<int64_t>(r) * I;
+  rem = rem < 0 ? 0 : (rem > I ? I : rem);
+  return static_cast<int>((w / cycle) * I + rem);
+}
 
 // Request owning row r: the b with qo_indptr[b] <= r < qo_indptr[b+1].
 __device__ __forceinline__ int find_request(const int32_t *ind, int B, int r) {
@@ -118,7 +129,7 @@ __global__ void plan_kernel(int B, int T, const int32_t *seq_lens, const int32_t
 // blocks row_blocks + b expand the shard's table for request b, sized by its
 // longest shard-local row.
 __global__ void shard_kernel(int B, int T, const int32_t *ind, const int32_t *row_len_global,
-                             int W, int rank, int32_t *row_len_local, TableArgs tab,
+                             int W, int rank, int I, int32_t *row_len_local, TableArgs tab,
                              int row_blocks, int *err) {
   const int total = ind[B];
   const bool ind_ok = ind[0] == 0 && total >= 0 && total <= T;
@@ -127,7 +138,7 @@ __global__ void shard_kernel(int B, int T, const int32_t *ind, const int32_t *ro
     int len = 0;
     const int r0 = ind[b], r1 = ind[b + 1];
     if (ind_ok && r0 >= 0 && r1 >= r0 && r1 <= T)
-      for (int r = r0; r < r1; ++r) len = max(len, rr_count(row_len_global[r], W, rank));
+      for (int r = r0; r < r1; ++r) len = max(len, il_count(row_len_global[r], W, rank, I));
     subpage_row(b, len, tab.bt, tab.bt_stride, tab.num_blocks, tab.block_size, tab.P, tab.sp,
                 tab.sp_stride, err);
     return;
@@ -135,7 +146,7 @@ __global__ void shard_kernel(int B, int T, const int32_t *ind, const int32_t *ro
   if (!ind_ok && blockIdx.x == 0 && threadIdx.x == 0) dev_error(err, MLA_DEV_BAD_INDPTR);
   const int stride = row_blocks * blockDim.x;
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < T; r += stride) {
-    row_len_local[r] = (ind_ok && r < total) ? rr_count(row_len_global[r], W, rank) : 0;
+    row_len_local[r] = (ind_ok && r < total) ? il_count(row_len_global[r], W, rank, I) : 0;
   }
 }
 
@@ -253,14 +264,14 @@ mla_status launch_plan_rows(int B, int T, const int32_t *seq_lens, const int32_t
 }
 
 mla_status launch_shard_rows(int B, int T, const int32_t *ind, const int32_t *row_len_global,
-                             int W, int rank, int32_t *row_len_local, const TableLaunch &t,
-                             int *err, cudaStream_t stream) {
+                             int W, int rank, int interleave, int32_t *row_len_local,
+                             const TableLaunch &t, int *err, cudaStream_t stream) {
   const int row_blocks = grid_for(T, 256);
   TableArgs tab{t.block_table, t.bt_stride, t.num_blocks, t.block_size, t.page_size,
                 t.subpage_table, t.sp_stride};
   const int blocks = row_blocks + (t.block_table != nullptr ? B : 0);
-  shard_kernel<<<blocks, 256, 0, stream>>>(B, T, ind, row_len_global, W, rank, row_len_local, tab,
-                                           row_blocks, err);
+  shard_kernel<<<blocks, 256, 0, stream>>>(B, T, ind, row_len_global, W, rank, interleave,
+                                           row_len_local, tab, row_blocks, err);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "shard_row_view launch");
 }
@@ -270,8 +281,10 @@ WorkspaceLayout decode_workspace_layout(const mla_decode_args &a) {
   size_t off = 0;
   if (a.num_segments > 1) {
     const size_t items = static_cast<size_t>(a.num_rows) * a.num_heads * a.num_segments;
+    const size_t row_blocks = (static_cast<size_t>(a.max_qlen) * a.num_heads + 63) / 64;
+    const size_t blocks = static_cast<size_t>(a.num_reqs) * row_blocks * a.num_segments;
     l.segm_out = off;
-    off += align256(items * 512 * sizeof(uint16_t));
+    off += align256(blocks * 512 * 64 * sizeof(uint16_t));
     l.segm_max = off;
     off += align256(items * sizeof(float));
     l.segm_sum = off;
@@ -361,12 +374,9 @@ mla_status mla_shard_row_view(int num_reqs, int num_rows, const int32_t *qo_indp
                               int interleave, int32_t *row_len_local, const int32_t *block_table,
                               int block_table_stride, int num_blocks, int block_size,
                               int32_t *subpage_table, int subpage_stride, mla_stream_t stream) {
-  if (interleave != 1) {
-    set_error("mla_shard_row_view: only round-robin interleave 1 is supported (got %d)", interleave);
-    return MLA_ERR_UNSUPPORTED;
-  }
-  if (world_size < 1 || rank < 0 || rank >= world_size) {
-    set_error("mla_shard_row_view: rank %d of world_size %d", rank, world_size);
+  if (world_size < 1 || rank < 0 || rank >= world_size || interleave < 1 ||
+      static_cast<int64_t>(interleave) * world_size > INT32_MAX) {
+    set_error("mla_shard_row_view: rank %d of world_size %d, interleave %d", rank, world_size, interleave);
     return MLA_ERR_INVALID_ARG;
   }
   if (num_reqs < 0 || num_rows < 0 || qo_indptr == nullptr ||
@@ -386,7 +396,7 @@ mla_status mla_shard_row_view(int num_reqs, int num_rows, const int32_t *qo_indp
   TableLaunch t{block_table, block_table_stride, num_blocks, block_size, P, subpage_table,
                 subpage_stride};
   return launch_shard_rows(num_reqs, num_rows, qo_indptr, row_len_global, world_size, rank,
-                           row_len_local, t, err, s);
+                           interleave, row_len_local, t, err, s);
 }
 
 static mla_status check_decode_args(const mla_decode_args *a) {
@@ -477,9 +487,11 @@ mla_status mla_decode_verify(const mla_decode_args *a, void *workspace, size_t w
   m.segm_out = d.segm_out;
   m.segm_max = d.segm_max;
   m.segm_sum = d.segm_sum;
+  m.qo_indptr = a->qo_indptr;
+  m.num_reqs = a->num_reqs;
+  m.row_blocks = (a->max_qlen * a->num_heads + 63) / 64;
   m.out = a->out;
   m.lse = a->lse;
-  m.live_rows = a->qo_indptr + a->num_reqs;
   return launch_merge(m, s);
 }
 
@@ -495,8 +507,12 @@ mla_status mla_merge_segments(const mla_merge_args *a, mla_stream_t stream) {
   }
   if (a->mode == MLA_MERGE_SEGMENTS) {
     if (a->segm_out == nullptr || a->segm_max == nullptr || a->segm_sum == nullptr ||
-        !is_aligned(a->segm_out, 16)) {
-      set_error("mla_merge_segments: segment mode needs 16-byte aligned segm_out, segm_max, segm_sum");
+        a->qo_indptr == nullptr || !is_aligned(a->segm_out, 16)) {
+      set_error("mla_merge_segments: segment mode needs 16-byte aligned segm_out, segm_max, segm_sum and qo_indptr");
+      return MLA_ERR_INVALID_ARG;
+    }
+    if (a->num_reqs < 0 || a->max_qlen < 1 || static_cast<int64_t>(a->max_qlen) * a->num_heads > INT32_MAX) {
+      set_error("mla_merge_segments: bad num_reqs %d / max_qlen %d", a->num_reqs, a->max_qlen);
       return MLA_ERR_INVALID_ARG;
     }
   } else if (a->mode == MLA_MERGE_STATES) {
@@ -520,11 +536,13 @@ mla_status mla_merge_segments(const mla_merge_args *a, mla_stream_t stream) {
   m.segm_out = a->segm_out;
   m.segm_max = a->segm_max;
   m.segm_sum = a->segm_sum;
+  m.qo_indptr = a->qo_indptr;
+  m.num_reqs = a->num_reqs;
+  m.row_blocks = a->mode == MLA_MERGE_SEGMENTS ? (a->max_qlen * a->num_heads + 63) / 64 : 0;
   m.part_out = a->part_out;
   m.part_lse = a->part_lse;
   m.out = a->out;
   m.lse = a->lse;
-  m.live_rows = nullptr;
   return launch_merge(m, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -70,6 +70,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 256;   // stage s: + 64 s
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
+constexpr long long kPvGrace = 1200;           // SM cycles a ready QK waits for a pending P^T
 constexpr float kLn2 = 0.69314718055994530942f;
 
 constexpr int kOffStages = 0;
@@ -79,7 +80,7 @@ constexpr int kOffMisc = kOffQ + kNumChunks * kQChunkBytes;
 // One claimed work item as published by the producer to the other roles.
 struct WorkEntry {
   int w;          // item index, -1 = no more work
-  int b, seg, q0, row_base, n_rows, seg_lo, seg_hi, n_tiles;
+  int b, rb, seg, q0, row_base, n_rows, seg_lo, seg_hi, n_tiles;
   alignas(16) int lens[kRows];  // visible tokens of each of the block's rows (0 past n_rows)
 };
 constexpr int kWorkRing = 4;
@@ -186,6 +187,7 @@ __device__ __forceinline__ bool decode_item(const Params &p, int w, WorkEntry &e
     const int seg_tokens = static_cast<int>((group_len + span - 1) / span) * p.page_size;
     e.w = w;
     e.b = b;
+    e.rb = rb;
     e.seg = seg;
     e.q0 = q0;
     e.n_rows = n_rows;
@@ -483,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t gq = 0, gp = 0, kq = 0, k = 0;  // tiles QK'd / PV'd, Q loads, work entries
       uint32_t first_bits = 0, k16_bits = 0;   // per S^T buffer: first tile of its item, 16-token steps
       int it_left = 0, it_i = 0, it_lo = 0, it_hi = 0;
+      uint32_t grace_g = 0xffffffffu;  // tile whose QK already waited for a pending PV
       bool q_ready = false, no_more = false;
       long long idle_since = clock64();
       while (true) {
@@ -532,6 +535,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else if (it_left > 0 && gq - gp < 2 &&
                    mbar_test(smem_u32(kFp8 ? &misc.ready[gq & 1u] : &misc.full[gq & 1u]), (gq >> 1) & 1u)) {
+          // The tensor pipe runs UMMAs in issue order, and QK of a tile keeps
+          // it busy for about a microsecond.  A PV whose P^T is about to be
+          // ready (the softmax of that tile is under way) goes first: it
+          // frees a stage for the next load.  Bounded grace period.
+          if (gp < gq && grace_g != gq) {
+            grace_g = gq;
+            const long long t0 = clock64();
+            while (!mbar_test(smem_u32(&misc.p_full[gp & 1u]), (gp >> 1) & 1u) && clock64() - t0 < kPvGrace) {
+            }
+            continue;  // back to the top: the PV branch takes it if it is ready
+          }
           tc_fence_after();
           const uint32_t st = gq & 1u;
           const uint32_t t_s = tmem + kTmemS + st * 64;
@@ -597,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(4, kNumSoftmaxWarps * 32);
       if (misc.sm_stop[k & 1u]) break;
       const WorkEntry &e = misc.work[ws];
-      const int n_rows = e.n_rows, n_tiles = e.n_tiles, seg = e.seg;
+      const int n_rows = e.n_rows, n_tiles = e.n_tiles, seg = e.seg, e_b = e.b, e_rb = e.rb;
       const int row_base = e.row_base, seg_lo = e.seg_lo, seg_hi = e.seg_hi;
       if (n_rows > 0 && n_tiles == 0) {
         // nothing visible in this segment for any row of the block
@@ -812,11 +826,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j)
             if (j < n_cols) o[static_cast<int64_t>(j) * 512] = __float2bfloat16_rn(__uint_as_float(ov[j]) * sc[j]);
         } else {
-          __nv_bfloat16 *o = p.segm_out + (r0 * S + seg) * 512 + dim;
-          const int64_t stride = static_cast<int64_t>(S) * 512;
+          // partial block (b, rb, seg), dim-major [512][64]: this thread's
+          // dim, the group's 32 rows as four 16-byte stores (a row that saw
+          // no token here gets 0)
+          uint4 *o = reinterpret_cast<uint4 *>(
+              p.segm_out + ((static_cast<int64_t>(e_b) * p.row_blocks + e_rb) * S + seg) * (512 * kRows) +
+              dim * kRows + 32 * g_col);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < n_cols && sc[j] != 0.0f) o[j * stride] = __float2bfloat16_rn(__uint_as_float(ov[j]) * sc[j]);
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int j = 8 * q + 2 * u;
+              const float lo = sc[j] != 0.0f ? __uint_as_float(ov[j]) * sc[j] : 0.0f;
+              const float hi = sc[j + 1] != 0.0f ? __uint_as_float(ov[j + 1]) * sc[j + 1] : 0.0f;
+              w4[u] = pack_bf16(lo, hi);
+            }
+            o[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
         }
       }
       tc_fence_before();  // O reads done before the next item's first PV overwrites O

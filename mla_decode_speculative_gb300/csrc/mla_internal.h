@@ -41,8 +41,8 @@ mla_status launch_plan_rows(int num_reqs, int num_rows, const int32_t *seq_lens,
                             const TableLaunch &table, int *err, cudaStream_t stream);
 mla_status launch_shard_rows(int num_reqs, int num_rows, const int32_t *qo_indptr,
                              const int32_t *row_len_global, int world_size, int rank,
-                             int32_t *row_len_local, const TableLaunch &table, int *err,
-                             cudaStream_t stream);
+                             int interleave, int32_t *row_len_local, const TableLaunch &table,
+                             int *err, cudaStream_t stream);
 
 struct DecodeLaunch {
   const mla_decode_args *a;
@@ -65,14 +65,16 @@ struct MergeLaunch {
   int num_rows;
   int num_heads;
   int num_parts;
-  const uint16_t *segm_out;  // bf16
+  const uint16_t *segm_out;  // bf16 blocks [B, RB, S, 512, 64]
   const float *segm_max;
   const float *segm_sum;
+  const int32_t *qo_indptr;  // segment mode
+  int num_reqs;              // segment mode
+  int row_blocks;            // segment mode: RB
   const void *part_out;
   const float *part_lse;
   void *out;
   float *lse;
-  const int32_t *live_rows;  // optional device int: rows (t) actually present; nullptr = all
 };
 mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream);
 

@@ -29,7 +29,7 @@ struct WriteParams {
   void *cache;
   int *err;
   int64_t cache_rows;
-  int num_reqs, num_rows, world_size, rank, bt_stride, num_blocks, block_size;
+  int num_reqs, num_rows, world_size, rank, interleave, bt_stride, num_blocks, block_size;
   float kv_scale;
   int fp8;
 };
@@ -61,8 +61,10 @@ __global__ void write_kv_kernel(const WriteParams p) {
       continue;
     }
     const int g = L - qlen + (r - p.qo_indptr[b]);
-    if (g % p.world_size != p.rank) continue;  // another shard owns this token
-    const int j = g / p.world_size;
+    // owner: runs of I positions dealt to the ranks in turn (I = 1: g mod W)
+    if ((g / p.interleave) % p.world_size != p.rank) continue;  // another shard owns this token
+    const int j = static_cast<int>((g / (static_cast<int64_t>(p.interleave) * p.world_size)) * p.interleave +
+                                   g % p.interleave);
     const int bi = j / p.block_size;
     const int blk = bi < p.bt_stride ? p.block_table[static_cast<int64_t>(b) * p.bt_stride + bi] : -1;
     const int64_t slot = static_cast<int64_t>(blk) * p.block_size + j % p.block_size;
@@ -107,11 +109,8 @@ extern "C" mla_status mla_write_kv(int num_reqs, int num_rows, const int32_t *se
                                    int block_table_stride, int num_blocks, int block_size,
                                    void *kv_cache, int kv_dtype, float kv_scale,
                                    int64_t num_cache_rows, mla_stream_t stream) {
-  if (interleave != 1) {
-    set_error("mla_write_kv: only round-robin interleave 1 is supported (got %d)", interleave);
-    return MLA_ERR_UNSUPPORTED;
-  }
   if (num_reqs < 0 || num_rows < 0 || world_size < 1 || rank < 0 || rank >= world_size ||
+      interleave < 1 || static_cast<int64_t>(interleave) * world_size > INT32_MAX ||
       block_size < 1 || block_table_stride < 1 || num_blocks < 1 || num_cache_rows < 1 ||
       (num_reqs > 0 && (seq_lens == nullptr || qo_indptr == nullptr || block_table == nullptr)) ||
       (num_rows > 0 && kv_new == nullptr) || kv_cache == nullptr) {
@@ -146,6 +145,7 @@ extern "C" mla_status mla_write_kv(int num_reqs, int num_rows, const int32_t *se
   p.num_rows = num_rows;
   p.world_size = world_size;
   p.rank = rank;
+  p.interleave = interleave;
   p.bt_stride = block_table_stride;
   p.num_blocks = num_blocks;
   p.block_size = block_size;

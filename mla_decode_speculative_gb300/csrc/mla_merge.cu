@@ -10,14 +10,18 @@
 // 评论区精华 4): W normalised shard states (out_r, lse_r) in base e:
 //   M = max lse_r, w_r = e^(lse_r - M), out = sum w_r out_r / sum w_r,
 //   lse = M + ln sum w_r.
-// An empty part (max / lse = -inf) is never read; all parts empty gives
-// out = 0, lse = -inf.
+// An empty part (max / lse = -inf) contributes nothing; all parts empty
+// gives out = 0, lse = -inf.
 //
-// Both modes read bf16 partial outputs (segment partials are stored in bf16
-// by the decode kernel).  HBM-bound streaming reduction: one 128-thread
-// block per (row, head); each thread owns 4 of the 512 output dims, reads
-// each live part with one 8-byte streaming load (8 parts in flight per
-// thread) and writes 8 bytes of bf16.
+// Segment partials come in the decode kernel's block layout: per (request,
+// 64-row block, segment) a dim-major [512][64] bf16 block.  One CTA merges
+// 64 output dims of one row block: lane l owns rows 2l and 2l+1, warp w dims
+// 8w..8w+7 of the CTA's 64, so every segment costs a warp eight coalesced
+// 128-byte loads (four segments in flight), with per-row weights staged in
+// shared memory; each thread writes one 16-byte piece of two rows.
+// State partials are row-major [W][T*H][512] bf16: one 128-thread block per
+// (row, head), thread t owning dims 4t..4t+3.  Both are HBM/L2 streaming
+// reductions.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -29,21 +33,31 @@
 namespace mla {
 namespace {
 
-constexpr int kThreadsPerItem = 128;  // 512 dims / 4 per thread
+constexpr int kThreadsPerItem = 128;  // state mode: 512 dims / 4 per thread
+constexpr int kBlockRows = 64;        // segment mode: rows per partial block
+constexpr int kDimsPerCta = 64;       // segment mode: output dims per CTA
 constexpr float kLn2 = 0.69314718055994530942f;
 
-struct MergeParams {
-  const __nv_bfloat16 *segm_out;
-  const float *segm_max;
-  const float *segm_sum;
+struct StateParams {
   const __nv_bfloat16 *part_out;
   const float *part_lse;
   __nv_bfloat16 *out;
   float *lse;
-  const int32_t *live_rows;
   int64_t num_items;  // rows * heads
+  int num_parts;
+};
+
+struct SegParams {
+  const __nv_bfloat16 *segm_out;  // [B, RB, S, 512, 64]
+  const float *segm_max;          // [T*H, S]
+  const float *segm_sum;
+  const int32_t *qo_indptr;
+  __nv_bfloat16 *out;
+  float *lse;
+  int num_rows;
   int num_heads;
   int num_parts;
+  int row_blocks;
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -60,39 +74,137 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
 }
-// Loads this thread's 4 dims of part s of item it.
-template <bool kSeg>
-__device__ __forceinline__ float4 load4(const MergeParams &p, int64_t it, int s, int tid) {
-  const __nv_bfloat16 *src = kSeg ? p.segm_out + (it * p.num_parts + s) * 512
-                                  : p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512;
-  const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(src) + tid);
-  return make_float4(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u),
-                     __uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// ---------------------------------------------------------------- segments
+constexpr int kSegChunk = 32;  // segments whose weights are staged at a time
+
+// grid (B * RB, 512 / 64), 256 threads.  The block's 64 rows x S statistics
+// are contiguous; the CTA stages per-row maxima, then normalised weights
+// 2^(m_s - M) / den for 32 segments at a time, in shared memory, and streams
+// the partial blocks four segments deep.
+__global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
+  __shared__ float s_w[kSegChunk][kBlockRows];
+  __shared__ int s_live[kSegChunk];
+  __shared__ float s_part[4][kBlockRows];
+  __shared__ float s_M[kBlockRows], s_inv[kBlockRows];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x / p.row_blocks, rb = blockIdx.x % p.row_blocks;
+  const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
+  if (q0 < 0 || q1 < q0 || q1 > p.num_rows) return;  // flagged by the decode kernel
+  const int rows_req = (q1 - q0) * p.num_heads;
+  const int n_rows = min(kBlockRows, rows_req - rb * kBlockRows);
+  if (n_rows <= 0) return;
+  const int S = p.num_parts;
+  const int64_t grow0 = static_cast<int64_t>(q0) * p.num_heads + rb * kBlockRows;  // first row of the block
+  const float *mx = p.segm_max + grow0 * S;  // [64 rows][S], contiguous
+  const float *sm = p.segm_sum + grow0 * S;
+
+  // per-row max and denominator: four threads per row, segments strided by 4
+  const int row = tid & (kBlockRows - 1), quarter = tid >> 6;
+  float M = -INFINITY;
+  if (row < n_rows)
+    for (int s = quarter; s < S; s += 4) M = fmaxf(M, mx[row * S + s]);
+  s_part[quarter][row] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_part[0][row], s_part[1][row]), fmaxf(s_part[2][row], s_part[3][row]));
+  __syncthreads();
+  float d = 0.0f;
+  if (row < n_rows && M != -INFINITY)
+    for (int s = quarter; s < S; s += 4) {
+      const float m = mx[row * S + s];
+      if (m != -INFINITY) d += exp2f(m - M) * sm[row * S + s];
+    }
+  s_part[quarter][row] = d;
+  __syncthreads();
+  if (quarter == 0) {
+    d = s_part[0][row] + s_part[1][row] + s_part[2][row] + s_part[3][row];
+    s_M[row] = M;
+    s_inv[row] = d > 0.0f ? 1.0f / d : 0.0f;
+    if (blockIdx.y == 0 && row < n_rows)
+      p.lse[grow0 + row] = d > 0.0f ? (M + log2f(d)) * kLn2 : -INFINITY;
+  }
+  __syncthreads();
+
+  const int dim0 = blockIdx.y * kDimsPerCta + warp * 8;
+  const int r0 = 2 * lane, r1 = 2 * lane + 1;  // this lane's rows of the block
+  float a0[8], a1[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a0[k] = a1[k] = 0.0f;
+  const int64_t blk0 = (static_cast<int64_t>(b) * p.row_blocks + rb) * S;
+  for (int c0 = 0; c0 < S; c0 += kSegChunk) {
+    const int nc = min(kSegChunk, S - c0);
+    // normalised weights of this chunk (0 for empty rows / segments / padding rows)
+    if (tid < kSegChunk) s_live[tid] = 0;
+    __syncthreads();
+    for (int i = tid; i < nc * kBlockRows; i += 256) {
+      const int sc = i / kBlockRows, rr = i % kBlockRows;
+      float w = 0.0f;
+      if (rr < n_rows && s_M[rr] != -INFINITY) {
+        const float m = mx[rr * S + c0 + sc];
+        if (m != -INFINITY) w = exp2f(m - s_M[rr]) * s_inv[rr];
+      }
+      s_w[sc][rr] = w;
+      if (w != 0.0f) s_live[sc] = 1;
+    }
+    __syncthreads();
+    for (int sc0 = 0; sc0 < nc; sc0 += 4) {
+      uint32_t x[4][8];
+      float w0[4], w1[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sc = sc0 + u;
+        const bool live = sc < nc && s_live[sc];
+        w0[u] = live ? s_w[sc][r0] : 0.0f;
+        w1[u] = live ? s_w[sc][r1] : 0.0f;
+        if (live) {
+          const uint32_t *src = reinterpret_cast<const uint32_t *>(
+              p.segm_out + ((blk0 + c0 + sc) * 512 + dim0) * kBlockRows) + lane;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) x[u][k] = __ldcs(src + k * (kBlockRows / 2));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) x[u][k] = 0u;
+        }
+      }
+      // a weight of 0 selects 0: an empty row's slot is never used as a value
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          a0[k] += (w0[u] != 0.0f) ? w0[u] * bf16_lo(x[u][k]) : 0.0f;
+          a1[k] += (w1[u] != 0.0f) ? w1[u] * bf16_hi(x[u][k]) : 0.0f;
+        }
+    }
+    __syncthreads();  // s_w / s_live are refilled by the next chunk
+  }
+  const int64_t g0 = grow0 + r0;
+  if (r0 < n_rows)
+    *reinterpret_cast<uint4 *>(p.out + g0 * 512 + dim0) =
+        make_uint4(pack_bf16(a0[0], a0[1]), pack_bf16(a0[2], a0[3]), pack_bf16(a0[4], a0[5]), pack_bf16(a0[6], a0[7]));
+  if (r1 < n_rows)
+    *reinterpret_cast<uint4 *>(p.out + (g0 + 1) * 512 + dim0) =
+        make_uint4(pack_bf16(a1[0], a1[1]), pack_bf16(a1[2], a1[3]), pack_bf16(a1[4], a1[5]), pack_bf16(a1[6], a1[7]));
+}
+
+// ---------------------------------------------------------------- states
+__device__ __forceinline__ float4 load_state4(const StateParams &p, int64_t it, int s, int tid) {
+  const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(
+                             p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512) + tid);
+  return make_float4(bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y));
 }
 
 // Up to 32 parts: no block barrier.  Every thread reads the item's (tiny,
-// L1-broadcast) statistics itself, so the loads of all live parts are issued
-// together, one dependent round trip after the statistics.
-template <bool kSeg>
-__global__ void __launch_bounds__(kThreadsPerItem) merge_kernel_small(const MergeParams p) {
+// L1-broadcast) LSEs itself, so the loads of all live parts are issued
+// together, one dependent round trip after the LSEs.
+__global__ void __launch_bounds__(kThreadsPerItem) merge_states_small(const StateParams p) {
   const int tid = threadIdx.x;
   const int64_t it = blockIdx.x;
-  if (p.live_rows != nullptr && it / p.num_heads >= static_cast<int64_t>(*p.live_rows)) return;
   const int n = p.num_parts;
-  float m[32], l[32];
+  float m[32];
 #pragma unroll
-  for (int s = 0; s < 32; ++s) {
-    m[s] = -INFINITY;
-    l[s] = 0.0f;
-    if (s < n) {
-      if constexpr (kSeg) {
-        m[s] = p.segm_max[it * n + s];
-        l[s] = p.segm_sum[it * n + s];
-      } else {
-        m[s] = p.part_lse[static_cast<int64_t>(s) * p.num_items + it];
-      }
-    }
-  }
+  for (int s = 0; s < 32; ++s) m[s] = (s < n) ? p.part_lse[static_cast<int64_t>(s) * p.num_items + it] : -INFINITY;
   float M = -INFINITY;
 #pragma unroll
   for (int s = 0; s < 32; ++s) M = fmaxf(M, m[s]);
@@ -105,15 +217,14 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel_small(const Merg
   float den = 0.0f;
 #pragma unroll
   for (int s = 0; s < 32; ++s) {
-    float w = 0.0f;
-    if (m[s] != -INFINITY) w = kSeg ? exp2f(m[s] - M) : expf(m[s] - M);
-    den += kSeg ? w * l[s] : w;
+    const float w = (m[s] != -INFINITY) ? expf(m[s] - M) : 0.0f;
+    den += w;
     m[s] = w;  // m now holds the weights
   }
   float4 v[32];
 #pragma unroll
   for (int s = 0; s < 32; ++s)
-    v[s] = (m[s] != 0.0f) ? load4<kSeg>(p, it, s, tid) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    v[s] = (m[s] != 0.0f) ? load_state4(p, it, s, tid) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int s = 0; s < 32; ++s) {
@@ -125,14 +236,12 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel_small(const Merg
   const float inv_den = 1.0f / den;
   *dst = make_uint2(pack_bf16(acc[0] * inv_den, acc[1] * inv_den),
                     pack_bf16(acc[2] * inv_den, acc[3] * inv_den));
-  if (tid == 0) p.lse[it] = kSeg ? (M + log2f(den)) * kLn2 : M + logf(den);
+  if (tid == 0) p.lse[it] = M + logf(den);
 }
 
-// One 128-thread block per (row, head): thread t owns output dims 4t..4t+3,
-// so every live part costs each thread one 8-byte load, and up to 8 parts
-// are in flight per thread.
-template <bool kSeg>
-__global__ void __launch_bounds__(kThreadsPerItem) merge_kernel(const MergeParams p) {
+// Any number of parts: live parts are compacted, in order, into shared
+// memory, then streamed with eight loads in flight per thread.
+__global__ void __launch_bounds__(kThreadsPerItem) merge_states(const StateParams p) {
   __shared__ float s_w[kMaxParts];
   __shared__ int s_idx[kMaxParts];
   __shared__ float s_red[kThreadsPerItem / 32];
@@ -140,14 +249,8 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel(const MergeParam
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int64_t it = blockIdx.x;
-  if (p.live_rows != nullptr && it / p.num_heads >= static_cast<int64_t>(*p.live_rows)) return;
   const int n = p.num_parts;
-
-  // statistic of part s: base-2 max (segments) or natural-log lse (states)
-  auto stat = [&](int s) -> float {
-    if constexpr (kSeg) return p.segm_max[it * n + s];
-    else return p.part_lse[static_cast<int64_t>(s) * p.num_items + it];
-  };
+  auto stat = [&](int s) -> float { return p.part_lse[static_cast<int64_t>(s) * p.num_items + it]; };
   float m_loc = -INFINITY;
   for (int s = tid; s < n; s += kThreadsPerItem) m_loc = fmaxf(m_loc, stat(s));
   m_loc = warp_max(m_loc);
@@ -157,15 +260,12 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel(const MergeParam
 #pragma unroll
   for (int k = 1; k < kThreadsPerItem / 32; ++k) M = fmaxf(M, s_red[k]);
   __syncthreads();
-
   uint2 *dst = reinterpret_cast<uint2 *>(p.out + it * 512) + tid;
   if (M == -INFINITY) {
     *dst = make_uint2(0, 0);
     if (tid == 0) p.lse[it] = -INFINITY;
     return;
   }
-  // unnormalised weights and the denominator; live parts are compacted, in
-  // order, into (s_idx, s_w) so the load loop below has no conditionals
   float d_loc = 0.0f;
   int n_live = 0;
   for (int base = 0; base < n; base += kThreadsPerItem) {
@@ -174,13 +274,8 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel(const MergeParam
     if (s < n) {
       const float m = stat(s);
       if (m != -INFINITY) {
-        if constexpr (kSeg) {
-          wgt = exp2f(m - M);
-          d_loc += wgt * p.segm_sum[it * n + s];
-        } else {
-          wgt = expf(m - M);
-          d_loc += wgt;
-        }
+        wgt = expf(m - M);
+        d_loc += wgt;
       }
     }
     const unsigned live = __ballot_sync(0xffffffffu, wgt != 0.0f);
@@ -203,62 +298,67 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_kernel(const MergeParam
 #pragma unroll
   for (int k = 0; k < kThreadsPerItem / 32; ++k) den += s_red[k];
   const float inv_den = 1.0f / den;
-
   float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   for (int k0 = 0; k0 < n_live; k0 += 8) {
-    float v[8][4];
+    float4 v[8];
     float wv[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int k = min(k0 + u, n_live - 1);  // padding re-reads the last live part, weight 0
-      const int s = s_idx[k];
       wv[u] = (k0 + u < n_live) ? s_w[k] : 0.0f;
-      const __nv_bfloat16 *src = kSeg ? p.segm_out + (it * n + s) * 512
-                                      : p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512;
-      const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(src) + tid);
-      v[u][0] = __uint_as_float(x.x << 16);
-      v[u][1] = __uint_as_float(x.x & 0xffff0000u);
-      v[u][2] = __uint_as_float(x.y << 16);
-      v[u][3] = __uint_as_float(x.y & 0xffff0000u);
+      v[u] = load_state4(p, it, s_idx[k], tid);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[c] = fmaf(wv[u], v[u][c], acc[c]);
+    for (int u = 0; u < 8; ++u) {
+      acc[0] = fmaf(wv[u], v[u].x, acc[0]);
+      acc[1] = fmaf(wv[u], v[u].y, acc[1]);
+      acc[2] = fmaf(wv[u], v[u].z, acc[2]);
+      acc[3] = fmaf(wv[u], v[u].w, acc[3]);
+    }
   }
   *dst = make_uint2(pack_bf16(acc[0] * inv_den, acc[1] * inv_den),
                     pack_bf16(acc[2] * inv_den, acc[3] * inv_den));
-  if (tid == 0) p.lse[it] = kSeg ? (M + log2f(den)) * kLn2 : M + logf(den);
+  if (tid == 0) p.lse[it] = M + logf(den);
 }
 
 }  // namespace
 
 mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
-  MergeParams p{};
-  p.segm_out = reinterpret_cast<const __nv_bfloat16 *>(m.segm_out);
-  p.segm_max = m.segm_max;
-  p.segm_sum = m.segm_sum;
-  p.part_out = static_cast<const __nv_bfloat16 *>(m.part_out);
-  p.part_lse = m.part_lse;
-  p.out = static_cast<__nv_bfloat16 *>(m.out);
-  p.lse = m.lse;
-  p.live_rows = m.live_rows;
-  p.num_items = static_cast<int64_t>(m.num_rows) * m.num_heads;
-  p.num_heads = m.num_heads;
-  p.num_parts = m.num_parts;
-  if (p.num_items == 0) return MLA_OK;
-  if (p.num_items > INT32_MAX) {
-    set_error("mla_merge_segments: too many (row, head) items");
-    return MLA_ERR_UNSUPPORTED;
-  }
-  const unsigned blocks = static_cast<unsigned>(p.num_items);
-  const bool small = p.num_parts <= 32;
   if (m.mode == MLA_MERGE_SEGMENTS) {
-    if (small) merge_kernel_small<true><<<blocks, kThreadsPerItem, 0, stream>>>(p);
-    else merge_kernel<true><<<blocks, kThreadsPerItem, 0, stream>>>(p);
+    if (m.num_reqs == 0 || m.num_rows == 0) return MLA_OK;
+    SegParams p{};
+    p.segm_out = reinterpret_cast<const __nv_bfloat16 *>(m.segm_out);
+    p.segm_max = m.segm_max;
+    p.segm_sum = m.segm_sum;
+    p.qo_indptr = m.qo_indptr;
+    p.out = static_cast<__nv_bfloat16 *>(m.out);
+    p.lse = m.lse;
+    p.num_rows = m.num_rows;
+    p.num_heads = m.num_heads;
+    p.num_parts = m.num_parts;
+    p.row_blocks = m.row_blocks;
+    const int64_t ctas = static_cast<int64_t>(m.num_reqs) * m.row_blocks;
+    if (ctas > INT32_MAX || m.row_blocks < 1) {
+      set_error("mla_merge_segments: bad row-block count (%lld)", (long long)ctas);
+      return MLA_ERR_UNSUPPORTED;
+    }
+    merge_segment_blocks<<<dim3(static_cast<unsigned>(ctas), 512 / kDimsPerCta), 256, 0, stream>>>(p);
   } else {
-    if (small) merge_kernel_small<false><<<blocks, kThreadsPerItem, 0, stream>>>(p);
-    else merge_kernel<false><<<blocks, kThreadsPerItem, 0, stream>>>(p);
+    StateParams p{};
+    p.part_out = static_cast<const __nv_bfloat16 *>(m.part_out);
+    p.part_lse = m.part_lse;
+    p.out = static_cast<__nv_bfloat16 *>(m.out);
+    p.lse = m.lse;
+    p.num_items = static_cast<int64_t>(m.num_rows) * m.num_heads;
+    p.num_parts = m.num_parts;
+    if (p.num_items == 0) return MLA_OK;
+    if (p.num_items > INT32_MAX) {
+      set_error("mla_merge_segments: too many (row, head) items");
+      return MLA_ERR_UNSUPPORTED;
+    }
+    const unsigned blocks = static_cast<unsigned>(p.num_items);
+    if (p.num_parts <= 32) merge_states_small<<<blocks, kThreadsPerItem, 0, stream>>>(p);
+    else merge_states<<<blocks, kThreadsPerItem, 0, stream>>>(p);
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");

@@ -61,7 +61,8 @@ class MergeArgs(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("num_rows", ctypes.c_int), ("num_heads", ctypes.c_int),
                 ("num_parts", ctypes.c_int), ("segm_out", ctypes.c_void_p),
                 ("segm_max", ctypes.c_void_p), ("segm_sum", ctypes.c_void_p),
-                ("part_out", ctypes.c_void_p), ("part_lse", ctypes.c_void_p),
+                ("qo_indptr", ctypes.c_void_p), ("num_reqs", ctypes.c_int),
+                ("max_qlen", ctypes.c_int), ("part_out", ctypes.c_void_p), ("part_lse", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
 
 
@@ -277,22 +278,33 @@ def decode_verify_noalloc(q, kv_cache, qo_indptr, row_len, subpage_table, page_s
     return out, lse
 
 
-def workspace_views(workspace: torch.Tensor, num_rows: int, num_heads: int, num_segments: int):
-    """The documented workspace layout: (segm_out [T,H,S,512], segm_max [T,H,S], segm_sum [T,H,S])."""
+def row_blocks(max_qlen: int, num_heads: int) -> int:
+    """RB: 64-row blocks per request in the segment-partial layout."""
+    return -(-max_qlen * num_heads // 64)
+
+
+def workspace_views(workspace: torch.Tensor, num_reqs: int, max_qlen: int, num_rows: int,
+                    num_heads: int, num_segments: int):
+    """The documented workspace layout: (segm_out [B, RB, S, 512, 64] bf16 blocks,
+    segm_max [T, H, S], segm_sum [T, H, S])."""
     items = num_rows * num_heads * num_segments
+    blocks = num_reqs * row_blocks(max_qlen, num_heads) * num_segments
     a256 = lambda x: (x + 255) & ~255
-    o_bytes = a256(items * 512 * 2)
+    o_bytes = a256(blocks * 512 * 64 * 2)
     m_bytes = a256(items * 4)
-    segm_out = workspace[:items * 512 * 2].view(torch.bfloat16).view(num_rows, num_heads, num_segments, 512)
+    segm_out = workspace[:blocks * 512 * 64 * 2].view(torch.bfloat16).view(
+        num_reqs, row_blocks(max_qlen, num_heads), num_segments, 512, 64)
     segm_max = workspace[o_bytes:o_bytes + items * 4].view(torch.float32).view(num_rows, num_heads, num_segments)
     segm_sum = workspace[o_bytes + m_bytes:o_bytes + m_bytes + items * 4].view(torch.float32).view(
         num_rows, num_heads, num_segments)
     return segm_out, segm_max, segm_sum
 
 
-def merge_segments(segm_out, segm_max, segm_sum, out=None, lse=None, stream=None):
-    """mla_merge_segments, segment mode: [T,H,S,512] bf16 + [T,H,S] f32 base-2 stats."""
-    T, H, S, dv = segm_out.shape
+def merge_segments(segm_out, segm_max, segm_sum, qo_indptr, max_qlen, out=None, lse=None,
+                   stream=None):
+    """mla_merge_segments, segment mode: bf16 partial blocks [B, RB, S, 512, 64] (the
+    decode workspace layout) + [T, H, S] f32 base-2 stats; qo_indptr [B + 1] int32."""
+    T, H, S = segm_max.shape
     if out is None:
         out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=segm_out.device)
     if lse is None:
@@ -300,6 +312,9 @@ def merge_segments(segm_out, segm_max, segm_sum, out=None, lse=None, stream=None
     m = MergeArgs()
     m.mode, m.num_rows, m.num_heads, m.num_parts = MLA_MERGE_SEGMENTS, T, H, S
     m.segm_out = _ptr(segm_out, torch.bfloat16, "segm_out")
+    m.qo_indptr = _ptr(qo_indptr, torch.int32, "qo_indptr")
+    m.num_reqs = int(qo_indptr.shape[0]) - 1
+    m.max_qlen = int(max_qlen)
     m.segm_max = _ptr(segm_max, torch.float32, "segm_max")
     m.segm_sum = _ptr(segm_sum, torch.float32, "segm_sum")
     m.out = _ptr(out, torch.bfloat16, "out")

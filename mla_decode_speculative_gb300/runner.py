@@ -22,12 +22,13 @@ class VerifyStep:
     def __init__(self, *, num_reqs: int, num_rows: int, num_heads: int, max_qlen: int,
                  block_size: int, num_blocks: int, block_table_width: int, max_kv_len: int,
                  num_segments: int = 1, world_size: int = 1, kv_fp8: bool = False,
-                 device="cuda"):
+                 interleave: int = 1, device="cuda"):
         self.B, self.T, self.H = num_reqs, num_rows, num_heads
         self.max_qlen = max_qlen
         self.block_size = block_size
         self.num_blocks = num_blocks
         self.W = world_size
+        self.interleave = interleave
         self.S = num_segments
         self.P = mla.page_size(block_size)
         self.sp_stride = max(1, -(-max_kv_len // self.P))
@@ -48,7 +49,8 @@ class VerifyStep:
         ws = 256  # scheduler state
         if num_segments > 1:
             items = num_rows * num_heads * num_segments
-            ws += ((items * 512 * 2 + 255) & ~255) + 2 * ((items * 4 + 255) & ~255)
+            blocks = num_reqs * mla.row_blocks(max_qlen, num_heads) * num_segments
+            ws += ((blocks * 512 * 64 * 2 + 255) & ~255) + 2 * ((items * 4 + 255) & ~255)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
 
     def __call__(self, q: torch.Tensor, kv_cache: torch.Tensor, seq_lens: torch.Tensor,
@@ -66,7 +68,7 @@ class VerifyStep:
         mla.plan_rows(seq_lens, qo_indptr, self.T, row_len=self.row_len, row_req=self.row_req,
                       stream=stream)
         for r in range(self.W):
-            mla.shard_row_view(qo_indptr, self.row_len, self.W, r, 1, block_tables[r],
+            mla.shard_row_view(qo_indptr, self.row_len, self.W, r, self.interleave, block_tables[r],
                                self.num_blocks, self.block_size, self.sp_stride,
                                row_len_local=self.row_len_local[r],
                                subpage_table=self.subpage[r], stream=stream)
@@ -85,7 +87,8 @@ def step_for_workload(wl, device="cuda", num_segments: Optional[int] = None) -> 
                       num_blocks=wl.num_blocks, block_table_width=wl.block_tables.shape[2],
                       max_kv_len=wl.max_kv_len,
                       num_segments=wl.num_segments if num_segments is None else num_segments,
-                      world_size=wl.world_size, kv_fp8=(wl.kv_dtype == "fp8"), device=device)
+                      world_size=wl.world_size, kv_fp8=(wl.kv_dtype == "fp8"),
+                      interleave=wl.interleave, device=device)
 
 
 def device_inputs(wl, device="cuda"):

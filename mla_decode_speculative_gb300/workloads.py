@@ -52,6 +52,7 @@ class Workload:
     sm_scale: float = SM_SCALE
     seed: int = 0
     max_kv_len: int = 0           # static bound on a row's tokens in one table's address space
+    interleave: int = 1           # round-robin run length of the context shards
 
     @property
     def num_reqs(self) -> int:
@@ -83,7 +84,8 @@ class Workload:
                 "qlen": sorted(set(int(x) for x in self.qlens)),
                 "seq_len_min": int(self.seq_lens.min()), "seq_len_max": int(self.seq_lens.max()),
                 "block_size": self.block_size, "kv_dtype": self.kv_dtype,
-                "world_size": self.world_size, "num_segments": self.num_segments}
+                "world_size": self.world_size, "num_segments": self.num_segments,
+                **({"interleave": self.interleave} if self.interleave != 1 else {})}
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -139,15 +141,17 @@ def _randn_fp8(shape, g: torch.Generator, device=None, chunk_rows=1 << 20):
 def make_workload(name: str, seq_lens, qlens, num_heads: int, block_size: int,
                   kv_dtype: str = "bf16", world_size: int = 1, num_segments: int = 1,
                   seed: int = 0, slack: float = 0.10, device=None,
-                  max_kv_len: Optional[int] = None) -> Workload:
+                  max_kv_len: Optional[int] = None, interleave: int = 1) -> Workload:
     """Draw a workload.  seq_lens / qlens: per-request ints (qlen <= seq_len)."""
     g = _gen(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     qlens = np.asarray(qlens, dtype=np.int32)
     B = seq_lens.shape[0]
     W = int(world_size)
-    # slots each request needs in one table's address space (ceil(L/W) per shard)
-    slots = [int(-(-int(L) // W)) for L in seq_lens]
+    # slots each request needs in one table's address space: at most I per
+    # started cycle of I * W positions on any shard (ceil(L/W) for I = 1)
+    I = int(interleave)
+    slots = [int(-(-int(L) // (I * W))) * I for L in seq_lens]
     blocks_per_req = [-(-s // block_size) for s in slots]
     max_blocks = max(1, max(blocks_per_req))
     used = W * sum(blocks_per_req)
@@ -176,7 +180,7 @@ def make_workload(name: str, seq_lens, qlens, num_heads: int, block_size: int,
                     block_size=block_size, kv_dtype=kv_dtype, world_size=W,
                     num_segments=num_segments, q=q, kv=kv, kv_scale=float(kv_scale),
                     block_tables=tables, num_blocks=num_blocks, seed=seed,
-                    max_kv_len=int(max_kv_len))
+                    max_kv_len=int(max_kv_len), interleave=I)
 
 
 # ---------------------------------------------------------------------------

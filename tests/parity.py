@@ -48,7 +48,7 @@ def oracle_reference(wl, sel=None):
                                 wl.block_tables[0], wl.block_size, sel=sel)
     out, lse, _, _ = oracle.sharded_attention(wl.qo_indptr, row_len, q, kv, wl.kv_scale,
                                               wl.sm_scale, wl.block_tables, wl.block_size,
-                                              wl.world_size, sel=sel)
+                                              wl.world_size, sel=sel, interleave=wl.interleave)
     return out, lse
 
 
@@ -74,3 +74,29 @@ def run_gpu(wl, num_segments=None, device="cuda"):
     out, lse = step(q, kv, seq, ind, bt, wl.sm_scale, wl.kv_scale)
     torch.cuda.synchronize()
     return out, lse, step
+
+
+def rows_to_blocks(x, qo_indptr, num_heads, row_blocks):
+    """[T, H, S, 512] per-(row, head) partials -> the decode workspace's block
+    layout [B, RB, S, 512, 64] (a request's rows t * H + h, 64 per block,
+    dim-major; unused rows left as NaN so that reading one would show)."""
+    T, H, S, D = x.shape
+    B = len(qo_indptr) - 1
+    out = np.full((B, row_blocks, S, D, 64), np.nan, dtype=x.dtype)
+    flat = x.reshape(T * H, S, D)
+    for b in range(B):
+        r0, r1 = int(qo_indptr[b]) * H, int(qo_indptr[b + 1]) * H
+        for i in range(r1 - r0):
+            out[b, i // 64, :, :, i % 64] = flat[r0 + i]
+    return out
+
+
+def blocks_to_rows(blocks, qo_indptr, num_heads, num_rows):
+    """Inverse of rows_to_blocks: [B, RB, S, 512, 64] -> [T, H, S, 512]."""
+    B, RB, S, D, _ = blocks.shape
+    out = np.zeros((num_rows * num_heads, S, D), dtype=blocks.dtype)
+    for b in range(B):
+        r0, r1 = int(qo_indptr[b]) * num_heads, int(qo_indptr[b + 1]) * num_heads
+        for i in range(r1 - r0):
+            out[r0 + i] = blocks[b, i // 64, :, :, i % 64]
+    return out.reshape(num_rows, num_heads, S, D)

@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
 def test_every_declared_symbol_is_exported(L):
     for n in declared_functions():
         assert hasattr(L, n), f"{n} declared in mla_gb300.h but not exported"
-    assert L.mla_abi_version() == 1
+    assert L.mla_abi_version() == 2
 
 
 def test_page_size_matches_rule(L):
@@ -50,9 +50,9 @@ def test_status_strings(L):
 
 def test_host_validation_without_cuda(L):
     vp = ctypes.c_void_p
-    # shard view: interleave != 1 is unsupported, checked before anything else
-    st = L.mla_shard_row_view(1, 1, vp(8), vp(8), 4, 0, 2, vp(8), None, 0, 0, 0, None, 0, None)
-    assert st == mla.MLA_ERR_UNSUPPORTED
+    # shard view: interleave < 1 is invalid, checked before anything else
+    st = L.mla_shard_row_view(1, 1, vp(8), vp(8), 4, 0, 0, vp(8), None, 0, 0, 0, None, 0, None)
+    assert st == mla.MLA_ERR_INVALID_ARG
     assert b"interleave" in L.mla_last_error_string()
     st = L.mla_shard_row_view(1, 1, vp(8), vp(8), 4, 4, 1, vp(8), None, 0, 0, 0, None, 0, None)
     assert st == mla.MLA_ERR_INVALID_ARG
@@ -84,9 +84,10 @@ def test_host_validation_without_cuda(L):
 
 def test_workspace_size_formula(L):
     a = mla.DecodeArgs()
-    a.num_rows, a.num_heads, a.num_segments = 128, 16, 16
+    a.num_reqs, a.max_qlen, a.num_rows, a.num_heads, a.num_segments = 40, 5, 128, 16, 16
     items = 128 * 16 * 16
+    blocks = 40 * 2 * 16  # RB = ceil(5 * 16 / 64) = 2 row blocks per request
     r256 = lambda x: (x + 255) // 256 * 256
-    assert L.mla_decode_verify_workspace(ctypes.byref(a)) == r256(items * 1024) + 2 * r256(items * 4) + 256
+    assert L.mla_decode_verify_workspace(ctypes.byref(a)) == r256(blocks * 512 * 64 * 2) + 2 * r256(items * 4) + 256
     a.num_segments = 1
     assert L.mla_decode_verify_workspace(ctypes.byref(a)) == 256

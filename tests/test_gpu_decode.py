@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from parity import assert_close, oracle_reference, run_gpu, sample_pairs
+from parity import assert_close, blocks_to_rows, oracle_reference, run_gpu, sample_pairs
 from mla_decode_speculative_gb300 import mla, workloads
 
 pytestmark = pytest.mark.gpu
@@ -64,6 +64,15 @@ def test_block_sizes_and_subpages(block_size):
     _full_check(wl, f"block_size {block_size}")
 
 
+@pytest.mark.parametrize("W,I", [(8, 4), (3, 16), (2, 64)])
+def test_dcp_interleaved_every_pair(W, I):
+    """Interleave I > 1 (runs of I positions dealt to the shards in turn):
+    row views, shard decodes and the state merge against the oracle."""
+    wl = workloads.make_workload("dcp_interleaved", [700, 90, 1500, 33], [4, 3, 8, 2], 16, 16,
+                                 world_size=W, num_segments=3, seed=W + I, interleave=I)
+    _full_check(wl, f"DCP W={W} interleave={I}")
+
+
 def test_many_rows_per_request_and_short_windows():
     # 32 heads x qlen 6 = 192 rows (three 64-row blocks); qlen == seq_len rows
     wl = workloads.make_workload("wide", [6, 300, 77], [6, 6, 5], 32, 16, num_segments=2, seed=9)
@@ -101,13 +110,14 @@ def test_nan_in_unused_cache_slots_is_never_read():
 def test_segment_partials_match_oracle():
     wl = workloads.verify_mtp4_bf16(seed=7, batch=3, lo=300, hi=1300, num_segments=5)
     out, lse, step = run_gpu(wl)
-    segm_out, segm_max, segm_sum = mla.workspace_views(step.workspace, wl.num_rows, wl.num_heads, 5)
+    segm_out, segm_max, segm_sum = mla.workspace_views(step.workspace, wl.num_reqs, int(wl.qlens.max()),
+                                                       wl.num_rows, wl.num_heads, 5)
     row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
     acc, mx, sm = oracle.segment_partials(wl.qo_indptr, row_len, wl.q_bits(), wl.kv_host(), 1.0,
                                           wl.sm_scale, wl.block_tables[0], wl.block_size, 5,
                                           oracle.page_size(wl.block_size))
     gm, gs = segm_max.cpu().numpy(), segm_sum.cpu().numpy()
-    go = segm_out.float().cpu().numpy()  # bf16 partial outputs
+    go = blocks_to_rows(segm_out.float().cpu().numpy(), wl.qo_indptr, wl.num_heads, wl.num_rows)  # bf16 blocks
     live = sm > 0
     assert (np.isneginf(gm) == ~live).all(), "GPU and oracle disagree on which segments are empty"
     # normalised segment output and segment LSE (invariant to the reference max)

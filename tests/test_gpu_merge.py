@@ -5,14 +5,17 @@ import pytest
 import torch
 
 import oracle
-from parity import assert_close
+from parity import assert_close, rows_to_blocks
 from mla_decode_speculative_gb300 import mla
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T,H,S", [(3, 16, 1), (128, 16, 16), (7, 12, 5), (2, 4, 40)])
-def test_merge_segments_matches_oracle(T, H, S):
+@pytest.mark.parametrize("qlens,H,S", [([1, 2], 16, 1), ([4] * 32, 16, 16), ([3, 1, 2, 1], 12, 5),
+                                       ([1, 1], 4, 40), ([8, 3], 16, 3)])
+def test_merge_segments_matches_oracle(qlens, H, S):
+    qo = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    T = int(qo[-1])
     rng = np.random.default_rng(T * 100 + S)
     acc = rng.standard_normal((T, H, S, 512)).astype(np.float32) * 20
     m = (rng.standard_normal((T, H, S)) * 4).astype(np.float32)
@@ -25,11 +28,15 @@ def test_merge_segments_matches_oracle(T, H, S):
         m[0, 0, :] = -np.inf  # a fully empty item
         l[0, 0, :] = 0
         acc[0, 0, :] = np.nan
-    # segment partial outputs are bf16; the oracle merges the same rounded values
-    acc_bf = torch.tensor(acc).to(torch.bfloat16)
-    out, lse = mla.merge_segments(acc_bf.to("cuda"), torch.tensor(m, device="cuda"),
-                                  torch.tensor(l, device="cuda"))
-    ref_o, ref_l = oracle.merge_segments(np.nan_to_num(acc_bf.float().numpy(), nan=0.0).astype(np.float64),
+    # segment partial outputs are bf16 in the decode workspace's block layout;
+    # the oracle merges the same rounded values
+    acc_r = torch.tensor(acc).to(torch.bfloat16).float().numpy()
+    RB = mla.row_blocks(max(qlens), H)
+    blocks = torch.tensor(rows_to_blocks(acc_r, qo, H, RB)).to(torch.bfloat16)
+    out, lse = mla.merge_segments(blocks.to("cuda"), torch.tensor(m, device="cuda"),
+                                  torch.tensor(l, device="cuda"), torch.tensor(qo, device="cuda"),
+                                  max(qlens))
+    ref_o, ref_l = oracle.merge_segments(np.nan_to_num(acc_r, nan=0.0).astype(np.float64),
                                          m.astype(np.float64), l.astype(np.float64))
     assert_close(out, lse, ref_o, ref_l, "segment merge")
     if S > 1:

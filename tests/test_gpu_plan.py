@@ -95,12 +95,32 @@ def test_shard_row_view_matches_oracle_and_sums(W):
     assert (total == o_rl).all()
 
 
-def test_shard_row_view_rejects_interleave_2():
+def test_shard_row_view_rejects_interleave_0():
     ind = _dev([0, 1])
     rl = _dev([5])
     with pytest.raises(mla.MLAError) as e:
-        mla.shard_row_view(ind, rl, 4, 0, interleave=2)
-    assert e.value.status == mla.MLA_ERR_UNSUPPORTED
+        mla.shard_row_view(ind, rl, 4, 0, interleave=0)
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("W,I", [(2, 2), (3, 4), (8, 16), (8, 1)])
+def test_shard_row_view_interleaved_matches_oracle(W, I):
+    rng = np.random.default_rng(W * 31 + I)
+    B = 24
+    seq = rng.integers(1, 6000, B).astype(np.int32)
+    ql = np.minimum(rng.integers(1, 9, B), seq).astype(np.int32)
+    ind = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    T = int(ind[-1])
+    o_rl, _, _ = oracle.plan_rows(seq, ind)
+    rl, _, _ = mla.plan_rows(_dev(seq), _dev(ind), T)
+    total = np.zeros(T, np.int64)
+    for r in range(W):
+        loc, _ = mla.shard_row_view(_dev(ind), rl, W, r, I)
+        assert mla.get_device_error() == 0
+        o_loc = oracle.shard_row_view(o_rl, W, r, I)
+        assert (loc.cpu().numpy() == o_loc).all()
+        total += o_loc
+    assert (total == o_rl).all()
 
 
 def test_device_checks_fire_without_faulting():

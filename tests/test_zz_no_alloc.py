@@ -53,17 +53,15 @@ def test_noalloc_matches_workspace_entry_point_twice(S):
 def test_noalloc_rejects_problems_beyond_the_static_scratch():
     wl = workloads.verify_mtp4_bf16(seed=22, batch=2, lo=100, hi=200, num_segments=1)
     q, kv, ind, step = _inputs(wl)
-    # 64 segments x 16 heads x a row capacity large enough to overflow 80 MiB
-    big_T = 1024
-    qb = torch.zeros((big_T, wl.num_heads, 576), dtype=torch.bfloat16, device="cuda")
-    rl = torch.zeros(big_T, dtype=torch.int32, device="cuda")
-    rl[:wl.num_rows] = step.row_len
-    a = mla.make_decode_args(qb, kv, ind, rl, step.subpage[0], step.P, 64, 4, wl.sm_scale,
-                             out=torch.empty((big_T, wl.num_heads, 512), dtype=torch.bfloat16,
+    # 1024 segments: the two requests' 64-row partial blocks alone take
+    # 2 x 1024 x 64 KiB = 128 MiB, beyond the 80 MiB of static scratch
+    S = 1024
+    a = mla.make_decode_args(q, kv, ind, step.row_len, step.subpage[0], step.P, S, 4, wl.sm_scale,
+                             out=torch.empty((wl.num_rows, wl.num_heads, 512), dtype=torch.bfloat16,
                                              device="cuda"),
-                             lse=torch.empty((big_T, wl.num_heads), dtype=torch.float32,
+                             lse=torch.empty((wl.num_rows, wl.num_heads), dtype=torch.float32,
                                              device="cuda"))
     assert mla.decode_verify_workspace_bytes(a) > mla.STATIC_SCRATCH_BYTES
     with pytest.raises(mla.MLAError) as e:
-        mla.decode_verify_noalloc(qb, kv, ind, rl, step.subpage[0], step.P, 64, 4, wl.sm_scale)
+        mla.decode_verify_noalloc(q, kv, ind, step.row_len, step.subpage[0], step.P, S, 4, wl.sm_scale)
     assert e.value.status == mla.MLA_ERR_WORKSPACE
