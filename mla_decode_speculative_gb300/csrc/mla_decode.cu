@@ -84,6 +84,7 @@ struct WorkEntry {
   alignas(16) int lens[kRows];  // visible tokens of each of the block's rows (0 past n_rows)
 };
 constexpr int kWorkRing = 4;
+constexpr int kMaxOrderedReqs = 128;  // requests ranked longest-first in every CTA
 
 struct Misc {
   uint64_t full[kStages];
@@ -98,6 +99,8 @@ struct Misc {
   int abort;
   WorkEntry work[kWorkRing];
   int sm_stop[2];  // softmax warps' shared exit decision (double-buffered)
+  int req_key[kMaxOrderedReqs];   // a request's longest row (producer's scratch)
+  int req_order[kMaxOrderedReqs]; // requests, longest first
   float red[2][2][4][32];  // [buffer][column group][lane quarter][lane]
 };
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc)) + 1024;
@@ -123,6 +126,7 @@ struct Params {
   int num_segments;
   int row_blocks;
   int num_items;           // num_reqs * row_blocks * num_segments
+  int num_reqs;
   int max_qlen;
   int num_rows;
   int max_len;
@@ -147,11 +151,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // then published with no rows).  Requests with more than 32 verify rows read
 // the extra lengths directly.
 __device__ __forceinline__ bool decode_item(const Params &p, int w, WorkEntry &e, int lane,
-                                            bool &clipped) {
+                                            bool &clipped, const int *order) {
   const int S = p.num_segments;
   const int seg = w % S;
   const int rb = (w / S) % p.row_blocks;
-  const int b = w / (S * p.row_blocks);
+  const int ob = w / (S * p.row_blocks);
+  const int b = order != nullptr ? order[ob] : ob;
   const int q0 = p.qo_indptr[b];
   const int q1 = p.qo_indptr[b + 1];
   clipped = false;
@@ -337,6 +342,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t armed = 0, armed_par = 0;
     uint32_t g = 0, kq = 0;  // running tile / Q-load counters
     bool ok = true;
+    // Longest items first (the tail of the dynamic schedule is set by the
+    // last long item claimed): with few enough requests every CTA ranks them
+    // by their longest row (a request's rows are nondecreasing, so its last
+    // row), ties by index, and claims in that order.
+    const int *order = nullptr;
+    if (p.num_reqs <= kMaxOrderedReqs) {
+      for (int b = lane; b < p.num_reqs; b += 32) {
+        const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
+        misc.req_key[b] = (q0 >= 0 && q1 > q0 && q1 <= p.num_rows) ? p.row_len[q1 - 1] : 0;
+      }
+      __syncwarp();
+      for (int b = lane; b < p.num_reqs; b += 32) {
+        const int key = misc.req_key[b];
+        int rank = 0;
+        for (int b2 = 0; b2 < p.num_reqs; ++b2) {
+          const int k2 = misc.req_key[b2];
+          rank += (k2 > key) || (k2 == key && b2 < b);
+        }
+        misc.req_order[rank] = b;
+      }
+      __syncwarp();
+      order = misc.req_order;
+    }
     for (uint32_t k = 0;; ++k) {
       const uint32_t ws = k % kWorkRing;
       WorkEntry &e = misc.work[ws];
@@ -357,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       bool clipped = false;
-      const bool good = decode_item(p, w, e, lane, clipped);
+      const bool good = decode_item(p, w, e, lane, clipped, order);
       __syncwarp();
       if (lane == 0) {
         if (!good) {
@@ -814,35 +842,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) sc[j] = __shfl_sync(0xffffffffu, col_scale, j);
       const int64_t r0 = row_base + 32 * g_col;
+      // O^T blocks two at a time: both TMEM loads in flight, one wait
 #pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {
-        uint32_t ov[32];
-        tmem_ld32(tmem + lane_addr + kTmemO + blk * kRows + 32 * g_col, ov);
-        if (!write) continue;
-        const int dim = blk * 128 + dim_lane;
-        if (direct) {
-          __nv_bfloat16 *o = p.out + r0 * 512 + dim;
+      for (int b2 = 0; b2 < 4; b2 += 2) {
+        uint32_t ovp[2][32];
+        tmem_ld32_async(tmem + lane_addr + kTmemO + b2 * kRows + 32 * g_col, ovp[0]);
+        tmem_ld32_async(tmem + lane_addr + kTmemO + (b2 + 1) * kRows + 32 * g_col, ovp[1]);
+        tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < n_cols) o[static_cast<int64_t>(j) * 512] = __float2bfloat16_rn(__uint_as_float(ov[j]) * sc[j]);
-        } else {
-          // partial block (b, rb, seg), dim-major [512][64]: this thread's
-          // dim, the group's 32 rows as four 16-byte stores (a row that saw
-          // no token here gets 0)
-          uint4 *o = reinterpret_cast<uint4 *>(
-              p.segm_out + ((static_cast<int64_t>(e_b) * p.row_blocks + e_rb) * S + seg) * (512 * kRows) +
-              dim * kRows + 32 * g_col);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int blk = b2 + h2;
+          const uint32_t (&ov)[32] = ovp[h2];
+          if (!write) continue;
+          const int dim = blk * 128 + dim_lane;
+          if (direct) {
+            __nv_bfloat16 *o = p.out + r0 * 512 + dim;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w4[4];
+            for (int j = 0; j < 32; ++j)
+              if (j < n_cols) o[static_cast<int64_t>(j) * 512] = __float2bfloat16_rn(__uint_as_float(ov[j]) * sc[j]);
+          } else {
+            // partial block (b, rb, seg), dim-major [512][64]: this thread's
+            // dim, the group's 32 rows as four 16-byte stores (a row that saw
+            // no token here gets 0)
+            uint4 *o = reinterpret_cast<uint4 *>(
+                p.segm_out + ((static_cast<int64_t>(e_b) * p.row_blocks + e_rb) * S + seg) * (512 * kRows) +
+                dim * kRows + 32 * g_col);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int j = 8 * q + 2 * u;
-              const float lo = sc[j] != 0.0f ? __uint_as_float(ov[j]) * sc[j] : 0.0f;
-              const float hi = sc[j + 1] != 0.0f ? __uint_as_float(ov[j + 1]) * sc[j + 1] : 0.0f;
-              w4[u] = pack_bf16(lo, hi);
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int j = 8 * q + 2 * u;
+                const float lo = sc[j] != 0.0f ? __uint_as_float(ov[j]) * sc[j] : 0.0f;
+                const float hi = sc[j + 1] != 0.0f ? __uint_as_float(ov[j + 1]) * sc[j + 1] : 0.0f;
+                w4[u] = pack_bf16(lo, hi);
+              }
+              o[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            o[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
       }
@@ -931,6 +967,7 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
     return MLA_ERR_UNSUPPORTED;
   }
   p.num_items = static_cast<int>(items);
+  p.num_reqs = a.num_reqs;
   p.max_qlen = a.max_qlen;
   p.num_rows = a.num_rows;
   p.max_len = a.subpage_stride * a.page_size;

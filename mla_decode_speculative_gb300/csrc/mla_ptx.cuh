@@ -244,6 +244,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "r"(taddr)
       : "memory");
 }
+// The same load without its wait: several loads can be in flight before one
+// tmem_wait_ld (the registers are valid only after it).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : MLA_R8(0), MLA_R8(8), MLA_R8(16), MLA_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // 16 TMEM lanes x 2 column halves: threads 0-15 read lanes base+0..15 at
 // columns col..col+15, threads 16-31 the same lanes at columns
 // col+16..col+31 (the second half is the immediate split offset), so a
