@@ -75,24 +75,31 @@ def kv_bytes(wl) -> int:
 
 
 def decode_unit_bytes(wl) -> dict:
-    """Algorithmic bytes of one launch of the decode kernel (unsharded):
-    visible KV rows, the query rows, and the split-K partials it must write
-    (an (m, l) pair for every (row, head, segment), a 1 KiB bf16 vector for
-    every (row, head, segment) that holds a visible token)."""
+    """Algorithmic bytes of one launch of the decode kernel (all shard views
+    of a sharded step in the one launch): visible KV rows, the query rows
+    (once per view), and the split-K partials it must write (an (m, l) pair
+    for every (view, row, head, segment), a 1 KiB bf16 vector for every one
+    that holds a visible token)."""
     P = min(128, wl.block_size & -wl.block_size)
     S = wl.num_segments
+    W, I = wl.world_size, wl.interleave
+
+    def local(w, r):  # positions of a window of w that shard r holds (runs of I dealt in turn)
+        rem = min(max(w % (I * W) - r * I, 0), I)
+        return (w // (I * W)) * I + rem
+
     active = 0
-    ind = wl.qo_indptr
-    for b in range(wl.num_reqs):
-        L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
-        tps_tok = -(-L // (S * P)) * P
-        for t in range(ql):
-            active += -(-(L - ql + 1 + t) // tps_tok)
+    for r in range(W):
+        for b in range(wl.num_reqs):
+            L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
+            tps_tok = max(1, -(-local(L, r) // (S * P))) * P
+            for t in range(ql):
+                active += -(-local(L - ql + 1 + t, r) // tps_tok)
     heads = wl.num_heads
     kv = kv_bytes(wl)
-    q = wl.num_rows * heads * 1152
-    partial = (wl.num_rows * heads * S * 8 + active * heads * 1024) if S > 1 else \
-        wl.num_rows * heads * (1024 + 4)
+    q = W * wl.num_rows * heads * 1152  # each shard view reads the queries
+    partial = (W * wl.num_rows * heads * S * 8 + active * heads * 1024) if S > 1 else \
+        W * wl.num_rows * heads * (1024 + 4)
     return {"kv": kv, "q": q, "partials": partial, "total": kv + q + partial}
 
 
@@ -318,12 +325,20 @@ def main():
 
     # decode kernel alone (partials only), for the roofline
     dgraph = None
-    if wl.world_size == 1 and wl.num_segments > 1:
+    if wl.num_segments > 1:
+        # the row plan / shard views of the warm-up steps stay in the step's buffers
+        W = wl.world_size
         dgraph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(dgraph, stream=stream):
-            mla.decode_verify(q, kv, ind, step.row_len, step.subpage[0], step.P, step.S,
-                              step.max_qlen, wl.sm_scale, wl.kv_scale, out=step.out, lse=step.lse,
-                              workspace=step.workspace, skip_merge=True)
+            if W == 1:
+                mla.decode_verify(q, kv, ind, step.row_len, step.subpage[0], step.P, step.S,
+                                  step.max_qlen, wl.sm_scale, wl.kv_scale, out=step.out,
+                                  lse=step.lse, workspace=step.workspace, skip_merge=True)
+            else:
+                mla.decode_verify(q, kv, ind, step.row_len_local, step.subpage, step.P, step.S,
+                                  step.max_qlen, wl.sm_scale, wl.kv_scale, out=step.part_out,
+                                  lse=step.part_lse, workspace=step.workspace, skip_merge=True,
+                                  num_views=W)
         torch.cuda.synchronize()
 
     def timed(g, n):
@@ -430,11 +445,11 @@ def main():
 
     kvb = kv_bytes(wl)
     value = world * kvb / (mean_ms * 1e-3) / 1e9
-    # plan (1) + decode (1) + segment merge (1 if S > 1); sharded: plan + W x
-    # (shard view + decode + segment merge) + state merge
+    # plan (1) + decode (1) + segment merge (1 if S > 1); sharded: plan + W
+    # shard views + one decode over the W views + segment merge + state merge
     per_decode = 2 if wl.num_segments > 1 else 1
     launches_per_step = (1 + per_decode if wl.world_size == 1 else
-                         1 + wl.world_size * (1 + per_decode) + 1)
+                         1 + wl.world_size + per_decode + 1)
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

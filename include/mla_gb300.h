@@ -162,6 +162,14 @@ typedef struct mla_decode_args {
   void *out;             /* [T, H, 512] bf16 output */
   float *lse;            /* [T, H] natural-log LSE (-inf for a row with no tokens) */
   int flags;             /* bitwise OR of mla_decode_flags (0 = default) */
+  /* V row views of the same queries in one call (0 or 1 = one view): view v
+   * reads row_len[v*T + r] and subpage_table[(v*B + b) * subpage_stride + p]
+   * and writes out[(v*T + r), h] / lse[(v*T + r), h] -- e.g. the W shard row
+   * views of one batch, whose outputs form the [W, T, H] shard states of the
+   * state merge.  row_len is [V, T], subpage_table [V, B, stride], out
+   * [V, T, H, 512], lse [V, T, H]; no counterpart in the pages, which run one
+   * decode per rank. */
+  int num_views;
 } mla_decode_args;
 
 typedef enum mla_decode_flags {
@@ -174,11 +182,11 @@ typedef enum mla_decode_flags {
 
 /* Workspace bytes mla_decode_verify needs for `a`.  Layout, each region
  * starting on a 256-byte boundary, in this order:
- *   segm_out [B, RB, S, 512, 64] bf16: RB = ceil(max_qlen * H / 64) row blocks
- *     per request; block (b, rb, s) holds, dim-major (64 rows innermost),
- *     segment s of request b's rows rb*64 .. rb*64 + 63, a request's rows
- *     numbered t * H + h; rows past the request's qlen * H are unused;
- *   segm_max [T, H, S] float32, segm_sum [T, H, S] float32
+ *   segm_out [V, B, RB, S, 512, 64] bf16: RB = ceil(max_qlen * H / 64) row
+ *     blocks per request; block (v, b, rb, s) holds, dim-major (64 rows
+ *     innermost), segment s of view v's rows rb*64 .. rb*64 + 63 of request b,
+ *     a request's rows numbered t * H + h; rows past qlen * H are unused;
+ *   segm_max [V, T, H, S] float32, segm_sum [V, T, H, S] float32
  *   (these three only when num_segments > 1), then 256 bytes of scheduler
  *   state (a work counter the call zeroes on the stream before its kernel).
  * Host only. */
@@ -232,6 +240,8 @@ typedef struct mla_merge_args {
   const int32_t *qo_indptr;  /* segment mode: [B + 1] device, as for mla_decode_verify */
   int num_reqs;              /* segment mode: B */
   int max_qlen;              /* segment mode: bound on qlen_b, fixes RB */
+  int num_views;             /* segment mode: V row views (0 or 1 = one); out / lse are
+                              * then [V, T, H, 512] / [V, T, H], the partials as above */
   /* MLA_MERGE_STATES: [W, T, H, 512] bf16 outputs and [W, T, H] float32
    * natural-log LSEs; a part with lse = -inf is empty and never read. */
   const void *part_out;

@@ -280,9 +280,10 @@ WorkspaceLayout decode_workspace_layout(const mla_decode_args &a) {
   WorkspaceLayout l{};
   size_t off = 0;
   if (a.num_segments > 1) {
-    const size_t items = static_cast<size_t>(a.num_rows) * a.num_heads * a.num_segments;
+    const size_t V = a.num_views > 1 ? a.num_views : 1;
+    const size_t items = V * a.num_rows * a.num_heads * a.num_segments;
     const size_t row_blocks = (static_cast<size_t>(a.max_qlen) * a.num_heads + 63) / 64;
-    const size_t blocks = static_cast<size_t>(a.num_reqs) * row_blocks * a.num_segments;
+    const size_t blocks = V * a.num_reqs * row_blocks * a.num_segments;
     l.segm_out = off;
     off += align256(blocks * 512 * 64 * sizeof(uint16_t));
     l.segm_max = off;
@@ -437,6 +438,11 @@ static mla_status check_decode_args(const mla_decode_args *a) {
     set_error("mla_decode_verify: q, kv_cache and out must be 16-byte aligned");
     return MLA_ERR_INVALID_ARG;
   }
+  if (a->num_views < 0 || static_cast<int64_t>(a->num_views > 1 ? a->num_views : 1) * a->num_rows * a->num_heads > INT32_MAX ||
+      static_cast<int64_t>(a->num_views > 1 ? a->num_views : 1) * a->num_reqs > INT32_MAX) {
+    set_error("mla_decode_verify: num_views %d (rows x heads x views must fit int32)", a->num_views);
+    return MLA_ERR_INVALID_ARG;
+  }
   if ((a->flags & ~MLA_DECODE_SKIP_MERGE) != 0) {
     set_error("mla_decode_verify: unknown flags 0x%x", a->flags);
     return MLA_ERR_INVALID_ARG;
@@ -489,6 +495,7 @@ mla_status mla_decode_verify(const mla_decode_args *a, void *workspace, size_t w
   m.segm_sum = d.segm_sum;
   m.qo_indptr = a->qo_indptr;
   m.num_reqs = a->num_reqs;
+  m.num_views = a->num_views > 1 ? a->num_views : 1;
   m.row_blocks = (a->max_qlen * a->num_heads + 63) / 64;
   m.out = a->out;
   m.lse = a->lse;
@@ -511,8 +518,11 @@ mla_status mla_merge_segments(const mla_merge_args *a, mla_stream_t stream) {
       set_error("mla_merge_segments: segment mode needs 16-byte aligned segm_out, segm_max, segm_sum and qo_indptr");
       return MLA_ERR_INVALID_ARG;
     }
-    if (a->num_reqs < 0 || a->max_qlen < 1 || static_cast<int64_t>(a->max_qlen) * a->num_heads > INT32_MAX) {
-      set_error("mla_merge_segments: bad num_reqs %d / max_qlen %d", a->num_reqs, a->max_qlen);
+    if (a->num_reqs < 0 || a->max_qlen < 1 || a->num_views < 0 ||
+        static_cast<int64_t>(a->max_qlen) * a->num_heads > INT32_MAX ||
+        static_cast<int64_t>(a->num_views > 1 ? a->num_views : 1) * a->num_rows * a->num_heads > INT32_MAX) {
+      set_error("mla_merge_segments: bad num_reqs %d / max_qlen %d / num_views %d", a->num_reqs, a->max_qlen,
+                a->num_views);
       return MLA_ERR_INVALID_ARG;
     }
   } else if (a->mode == MLA_MERGE_STATES) {
@@ -538,6 +548,7 @@ mla_status mla_merge_segments(const mla_merge_args *a, mla_stream_t stream) {
   m.segm_sum = a->segm_sum;
   m.qo_indptr = a->qo_indptr;
   m.num_reqs = a->num_reqs;
+  m.num_views = a->num_views > 1 ? a->num_views : 1;
   m.row_blocks = a->mode == MLA_MERGE_SEGMENTS ? (a->max_qlen * a->num_heads + 63) / 64 : 0;
   m.part_out = a->part_out;
   m.part_lse = a->part_lse;

@@ -80,7 +80,7 @@ constexpr int kOffMisc = kOffQ + kNumChunks * kQChunkBytes;
 // One claimed work item as published by the producer to the other roles.
 struct WorkEntry {
   int w;          // item index, -1 = no more work
-  int b, rb, seg, q0, row_base, n_rows, seg_lo, seg_hi, n_tiles;
+  int b, rb, seg, q_row, row_base, n_rows, seg_lo, seg_hi, n_tiles;  // b: view * B + request
   alignas(16) int lens[kRows];  // visible tokens of each of the block's rows (0 past n_rows)
 };
 constexpr int kWorkRing = 4;
@@ -125,8 +125,9 @@ struct Params {
   int num_heads;
   int num_segments;
   int row_blocks;
-  int num_items;           // num_reqs * row_blocks * num_segments
+  int num_items;           // num_reqs * num_views * row_blocks * num_segments
   int num_reqs;
+  int num_views;           // row views of the same queries decoded in one launch
   int max_qlen;
   int num_rows;
   int max_len;
@@ -155,8 +156,11 @@ __device__ __forceinline__ bool decode_item(const Params &p, int w, WorkEntry &e
   const int S = p.num_segments;
   const int seg = w % S;
   const int rb = (w / S) % p.row_blocks;
-  const int ob = w / (S * p.row_blocks);
+  // item order: request (longest first), then view, row block, segment
+  const int v = (w / (S * p.row_blocks)) % p.num_views;
+  const int ob = w / (S * p.row_blocks * p.num_views);
   const int b = order != nullptr ? order[ob] : ob;
+  const int vrow = v * p.num_rows;  // view v's rows start here in row_len / out / lse
   const int q0 = p.qo_indptr[b];
   const int q1 = p.qo_indptr[b + 1];
   clipped = false;
@@ -167,10 +171,10 @@ __device__ __forceinline__ bool decode_item(const Params &p, int w, WorkEntry &e
   const int n_rows = row_begin < rows_req ? min(kRows, rows_req - row_begin) : 0;
   // lengths of the request's rows: lane t holds row t (t < 32)
   int my_len = 0;
-  if (lane < qlen) my_len = p.row_len[q0 + lane];
+  if (lane < qlen) my_len = p.row_len[vrow + q0 + lane];
   int group_len = 0;
   for (int t = lane; t < qlen; t += 32) {
-    int l = t == lane ? my_len : p.row_len[q0 + t];
+    int l = t == lane ? my_len : p.row_len[vrow + q0 + t];
     if (l > p.max_len) { clipped = true; l = p.max_len; }
     group_len = max(group_len, max(l, 0));
   }
@@ -184,19 +188,19 @@ __device__ __forceinline__ bool decode_item(const Params &p, int w, WorkEntry &e
     const int t = (row_begin + c) / p.num_heads;
     const int tt = t < 32 ? t : 0;
     int l = __shfl_sync(0xffffffffu, my_len, tt);
-    if (t >= 32 && c < n_rows) l = p.row_len[q0 + t];
+    if (t >= 32 && c < n_rows) l = p.row_len[vrow + q0 + t];
     e.lens[c] = c < n_rows ? min(max(l, 0), p.max_len) : 0;
   }
   if (lane == 0) {
     const long long span = static_cast<long long>(S) * p.page_size;
     const int seg_tokens = static_cast<int>((group_len + span - 1) / span) * p.page_size;
     e.w = w;
-    e.b = b;
+    e.b = v * p.num_reqs + b;
     e.rb = rb;
     e.seg = seg;
-    e.q0 = q0;
+    e.q_row = q0 * p.num_heads + row_begin;
     e.n_rows = n_rows;
-    e.row_base = q0 * p.num_heads + row_begin;
+    e.row_base = (vrow + q0) * p.num_heads + row_begin;
     e.seg_lo = seg * seg_tokens;
     e.seg_hi = min(e.seg_lo + seg_tokens, group_len);
     e.n_tiles = (n_rows > 0 && e.seg_lo < e.seg_hi) ? (e.seg_hi - e.seg_lo + kTileTok - 1) / kTileTok : 0;
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int n_tiles = __shfl_sync(0xffffffffu, lane == 0 ? e.n_tiles : 0, 0);
       if (n_tiles > 0) {
-        const int seg_lo = e.seg_lo, seg_hi = e.seg_hi, row_base = e.row_base;
+        const int seg_lo = e.seg_lo, seg_hi = e.seg_hi, q_row = e.q_row;
         // Sub-page ids are read 32 at a time (lane l holds page win_base + l),
         // ahead of the waits, so no id fetch sits between a freed stage and
         // its next copies.
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive_expect_tx(q_bar, kNumChunks * kQChunkBytes);
           __syncwarp();
           if (lane < kNumChunks)
-            tma_load_2d(s_q + lane * kQChunkBytes, &tm_q, q_bar, lane * 64, row_base, pol_q);
+            tma_load_2d(s_q + lane * kQChunkBytes, &tm_q, q_bar, lane * 64, q_row, pol_q);
         }
         ++kq;
         for (int i = 0; i < n_tiles && ok; ++i, ++g) {
@@ -961,13 +965,15 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
   p.num_heads = a.num_heads;
   p.num_segments = a.num_segments;
   p.row_blocks = (a.max_qlen * a.num_heads + kRows - 1) / kRows;
-  const int64_t items = static_cast<int64_t>(a.num_reqs) * p.row_blocks * a.num_segments;
+  const int V = a.num_views > 1 ? a.num_views : 1;
+  const int64_t items = static_cast<int64_t>(a.num_reqs) * V * p.row_blocks * a.num_segments;
   if (items > INT32_MAX) {
     set_error("mla_decode_verify: too many work items (%lld)", (long long)items);
     return MLA_ERR_UNSUPPORTED;
   }
   p.num_items = static_cast<int>(items);
   p.num_reqs = a.num_reqs;
+  p.num_views = V;
   p.max_qlen = a.max_qlen;
   p.num_rows = a.num_rows;
   p.max_len = a.subpage_stride * a.page_size;

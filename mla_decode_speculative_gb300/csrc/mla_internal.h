@@ -70,6 +70,7 @@ struct MergeLaunch {
   const float *segm_sum;
   const int32_t *qo_indptr;  // segment mode
   int num_reqs;              // segment mode
+  int num_views;             // segment mode: V row views (>= 1)
   int row_blocks;            // segment mode: RB
   const void *part_out;
   const float *part_lse;

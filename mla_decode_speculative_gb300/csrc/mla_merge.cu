@@ -58,6 +58,7 @@ struct SegParams {
   int num_heads;
   int num_parts;
   int row_blocks;
+  int num_reqs;
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -90,14 +91,16 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
   __shared__ float s_part[4][kBlockRows];
   __shared__ float s_M[kBlockRows], s_inv[kBlockRows];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x / p.row_blocks, rb = blockIdx.x % p.row_blocks;
+  // block (view, request, row block): vb = v * B + b
+  const int vb = blockIdx.x / p.row_blocks, rb = blockIdx.x % p.row_blocks;
+  const int v = vb / p.num_reqs, b = vb % p.num_reqs;
   const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
   if (q0 < 0 || q1 < q0 || q1 > p.num_rows) return;  // flagged by the decode kernel
   const int rows_req = (q1 - q0) * p.num_heads;
   const int n_rows = min(kBlockRows, rows_req - rb * kBlockRows);
   if (n_rows <= 0) return;
   const int S = p.num_parts;
-  const int64_t grow0 = static_cast<int64_t>(q0) * p.num_heads + rb * kBlockRows;  // first row of the block
+  const int64_t grow0 = (static_cast<int64_t>(v) * p.num_rows + q0) * p.num_heads + rb * kBlockRows;  // first row
   const float *mx = p.segm_max + grow0 * S;  // [64 rows][S], contiguous
   const float *sm = p.segm_sum + grow0 * S;
 
@@ -132,7 +135,7 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
   float a0[8], a1[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) a0[k] = a1[k] = 0.0f;
-  const int64_t blk0 = (static_cast<int64_t>(b) * p.row_blocks + rb) * S;
+  const int64_t blk0 = (static_cast<int64_t>(vb) * p.row_blocks + rb) * S;
   for (int c0 = 0; c0 < S; c0 += kSegChunk) {
     const int nc = min(kSegChunk, S - c0);
     // normalised weights of this chunk (0 for empty rows / segments / padding rows)
@@ -337,7 +340,8 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
     p.num_heads = m.num_heads;
     p.num_parts = m.num_parts;
     p.row_blocks = m.row_blocks;
-    const int64_t ctas = static_cast<int64_t>(m.num_reqs) * m.row_blocks;
+    p.num_reqs = m.num_reqs;
+    const int64_t ctas = static_cast<int64_t>(m.num_reqs) * m.num_views * m.row_blocks;
     if (ctas > INT32_MAX || m.row_blocks < 1) {
       set_error("mla_merge_segments: bad row-block count (%lld)", (long long)ctas);
       return MLA_ERR_UNSUPPORTED;

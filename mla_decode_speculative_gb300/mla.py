@@ -54,7 +54,8 @@ class DecodeArgs(ctypes.Structure):
                 ("qo_indptr", ctypes.c_void_p), ("row_len", ctypes.c_void_p),
                 ("subpage_table", ctypes.c_void_p), ("subpage_stride", ctypes.c_int),
                 ("page_size", ctypes.c_int), ("num_segments", ctypes.c_int),
-                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("flags", ctypes.c_int)]
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("flags", ctypes.c_int),
+                ("num_views", ctypes.c_int)]
 
 
 class MergeArgs(ctypes.Structure):
@@ -62,7 +63,7 @@ class MergeArgs(ctypes.Structure):
                 ("num_parts", ctypes.c_int), ("segm_out", ctypes.c_void_p),
                 ("segm_max", ctypes.c_void_p), ("segm_sum", ctypes.c_void_p),
                 ("qo_indptr", ctypes.c_void_p), ("num_reqs", ctypes.c_int),
-                ("max_qlen", ctypes.c_int), ("part_out", ctypes.c_void_p), ("part_lse", ctypes.c_void_p),
+                ("max_qlen", ctypes.c_int), ("num_views", ctypes.c_int), ("part_out", ctypes.c_void_p), ("part_lse", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
 
 
@@ -200,7 +201,8 @@ def shard_row_view(qo_indptr: torch.Tensor, row_len_global: torch.Tensor, world_
 
 
 def make_decode_args(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_, num_segments,
-                     max_qlen, sm_scale, kv_scale=1.0, out=None, lse=None, flags=0) -> DecodeArgs:
+                     max_qlen, sm_scale, kv_scale=1.0, out=None, lse=None, flags=0,
+                     num_views=1) -> DecodeArgs:
     T, H, dk = q.shape
     if dk != D_QK:
         raise ValueError("q must be [T, H, 576]")
@@ -221,12 +223,13 @@ def make_decode_args(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_,
     a.qo_indptr = _ptr(qo_indptr, torch.int32, "qo_indptr")
     a.row_len = _ptr(row_len, torch.int32, "row_len")
     a.subpage_table = _ptr(subpage_table, torch.int32, "subpage_table")
-    a.subpage_stride = int(subpage_table.shape[1])
+    a.subpage_stride = int(subpage_table.shape[-1])
     a.page_size = int(page_size_)
     a.num_segments = int(num_segments)
     a.out = _ptr(out, torch.bfloat16, "out")
     a.lse = _ptr(lse, torch.float32, "lse")
     a.flags = int(flags)
+    a.num_views = int(num_views)
     return a
 
 
@@ -236,17 +239,21 @@ def decode_verify_workspace_bytes(a: DecodeArgs) -> int:
 
 def decode_verify(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_, num_segments,
                   max_qlen, sm_scale, kv_scale=1.0, out=None, lse=None, workspace=None,
-                  stream=None, skip_merge=False):
+                  stream=None, skip_merge=False, num_views=1):
     """mla_decode_verify.  Returns (out [T, H, 512] bf16, lse [T, H] f32, workspace).
-    skip_merge: leave the segment partials in the workspace (MLA_DECODE_SKIP_MERGE)."""
+    skip_merge: leave the segment partials in the workspace (MLA_DECODE_SKIP_MERGE).
+    num_views V > 1: row_len [V, T], subpage_table [V, B, stride]; out [V, T, H, 512],
+    lse [V, T, H] (V row views of the same queries, one launch)."""
     T, H, _ = q.shape
+    V = max(1, int(num_views))
+    lead = (V, T) if V > 1 else (T,)
     if out is None:
-        out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((*lead, H, D_V), dtype=torch.bfloat16, device=q.device)
     if lse is None:
-        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+        lse = torch.empty((*lead, H), dtype=torch.float32, device=q.device)
     a = make_decode_args(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_,
                          num_segments, max_qlen, sm_scale, kv_scale, out, lse,
-                         MLA_DECODE_SKIP_MERGE if skip_merge else 0)
+                         MLA_DECODE_SKIP_MERGE if skip_merge else 0, num_views=V)
     need = decode_verify_workspace_bytes(a)
     if need and (workspace is None or workspace.numel() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -284,9 +291,10 @@ def row_blocks(max_qlen: int, num_heads: int) -> int:
 
 
 def workspace_views(workspace: torch.Tensor, num_reqs: int, max_qlen: int, num_rows: int,
-                    num_heads: int, num_segments: int):
-    """The documented workspace layout: (segm_out [B, RB, S, 512, 64] bf16 blocks,
-    segm_max [T, H, S], segm_sum [T, H, S])."""
+                    num_heads: int, num_segments: int, num_views: int = 1):
+    """The documented workspace layout (num_views = 1): (segm_out [B, RB, S, 512, 64] bf16
+    blocks, segm_max [T, H, S], segm_sum [T, H, S]); V views stack V such layouts."""
+    num_reqs, num_rows = num_reqs * num_views, num_rows * num_views
     items = num_rows * num_heads * num_segments
     blocks = num_reqs * row_blocks(max_qlen, num_heads) * num_segments
     a256 = lambda x: (x + 255) & ~255

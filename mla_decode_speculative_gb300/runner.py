@@ -6,8 +6,8 @@ bounds, so a step issues only library launches and can be captured in a CUDA
 graph.  Unsharded step: mla_plan_rows (+ sub-page expansion) ->
 mla_decode_verify (decode + segment merge).  Context-sharded step (W round-robin
 shards simulated on one device): mla_plan_rows (global windows) -> per shard
-mla_shard_row_view + mla_decode_verify into a [W, T, H, .] state buffer ->
-mla_merge_segments (state mode).
+mla_shard_row_view -> one mla_decode_verify over the W row views (num_views = W)
+into a [W, T, H, .] state buffer -> mla_merge_segments (state mode).
 """
 from __future__ import annotations
 
@@ -48,8 +48,8 @@ class VerifyStep:
                                         device=dev)
         ws = 256  # scheduler state
         if num_segments > 1:
-            items = num_rows * num_heads * num_segments
-            blocks = num_reqs * mla.row_blocks(max_qlen, num_heads) * num_segments
+            items = world_size * num_rows * num_heads * num_segments
+            blocks = world_size * num_reqs * mla.row_blocks(max_qlen, num_heads) * num_segments
             ws += ((blocks * 512 * 64 * 2 + 255) & ~255) + 2 * ((items * 4 + 255) & ~255)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
 
@@ -72,10 +72,10 @@ class VerifyStep:
                                self.num_blocks, self.block_size, self.sp_stride,
                                row_len_local=self.row_len_local[r],
                                subpage_table=self.subpage[r], stream=stream)
-            mla.decode_verify(q, kv_cache, qo_indptr, self.row_len_local[r], self.subpage[r],
-                              self.P, self.S, self.max_qlen, sm_scale, kv_scale,
-                              out=self.part_out[r], lse=self.part_lse[r],
-                              workspace=self.workspace, stream=stream)
+        # all W shard views in one decode launch, straight into the shard states
+        mla.decode_verify(q, kv_cache, qo_indptr, self.row_len_local, self.subpage, self.P, self.S,
+                          self.max_qlen, sm_scale, kv_scale, out=self.part_out, lse=self.part_lse,
+                          workspace=self.workspace, stream=stream, num_views=self.W)
         mla.merge_states(self.part_out, self.part_lse, out=self.out, lse=self.lse, stream=stream)
         return self.out, self.lse
 
