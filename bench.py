@@ -346,6 +346,9 @@ def main():
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         with torch.cuda.stream(stream):
             for k in range(n):
+                # a ~50 us device spin ahead of the flush keeps the launch queue
+                # ahead of the GPU, so no host-side delay falls inside a bracket
+                torch.cuda._sleep(100000)
                 flush.zero_()
                 starts[k].record(stream)
                 g.replay()

@@ -71,6 +71,7 @@ constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 256;   // stage s: + 64 s
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr long long kPvGrace = 1200;           // SM cycles a ready QK waits for a pending P^T
+constexpr long long kPvGraceLast = 20000;      // ... when that P^T is an item's last (its epilogue waits)
 constexpr float kLn2 = 0.69314718055994530942f;
 
 constexpr int kOffStages = 0;
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // landed and an S^T buffer is free (at most two tiles between QK and
       // PV).  Polling uses non-blocking barrier tests.
       uint32_t gq = 0, gp = 0, kq = 0, k = 0;  // tiles QK'd / PV'd, Q loads, work entries
-      uint32_t first_bits = 0, k16_bits = 0;   // per S^T buffer: first tile of its item, 16-token steps
+      uint32_t first_bits = 0, last_bits = 0, k16_bits = 0;  // per S^T buffer: first / last tile of its item, 16-token steps
       int it_left = 0, it_i = 0, it_lo = 0, it_hi = 0;
       uint32_t grace_g = 0xffffffffu;  // tile whose QK already waited for a pending PV
       bool q_ready = false, no_more = false;
@@ -573,8 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // frees a stage for the next load.  Bounded grace period.
           if (gp < gq && grace_g != gq) {
             grace_g = gq;
+            const long long grace = ((last_bits >> (gp & 1u)) & 1u) ? kPvGraceLast : kPvGrace;
             const long long t0 = clock64();
-            while (!mbar_test(smem_u32(&misc.p_full[gp & 1u]), (gp >> 1) & 1u) && clock64() - t0 < kPvGrace) {
+            while (!mbar_test(smem_u32(&misc.p_full[gp & 1u]), (gp >> 1) & 1u) && clock64() - t0 < grace) {
             }
             continue;  // back to the top: the PV branch takes it if it is ready
           }
@@ -596,6 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(smem_u32(&misc.s_full[st]));
           const int n_valid = min(kTileTok, it_hi - (it_lo + it_i * kTileTok));
           first_bits = (first_bits & ~(1u << st)) | (static_cast<uint32_t>(it_i == 0) << st);
+          last_bits = (last_bits & ~(1u << st)) | (static_cast<uint32_t>(it_left == 1) << st);
           k16_bits = (k16_bits & ~(15u << (4 * st))) | (static_cast<uint32_t>((n_valid + 15) / 16) << (4 * st));
           ++gq;
           ++it_i;

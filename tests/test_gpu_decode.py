@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from parity import assert_close, blocks_to_rows, oracle_reference, run_gpu, sample_pairs
-from mla_decode_speculative_gb300 import mla, workloads
+from mla_decode_speculative_gb300 import mla, runner, workloads
 
 pytestmark = pytest.mark.gpu
 
@@ -71,6 +71,28 @@ def test_dcp_interleaved_every_pair(W, I):
     wl = workloads.make_workload("dcp_interleaved", [700, 90, 1500, 33], [4, 3, 8, 2], 16, 16,
                                  world_size=W, num_segments=3, seed=W + I, interleave=I)
     _full_check(wl, f"DCP W={W} interleave={I}")
+
+
+@pytest.mark.parametrize("S", [1, 3])
+def test_row_views_in_one_launch_equal_separate_calls(S):
+    """num_views = W decodes the W shard row views in one launch; every view's
+    output must equal, bit for bit, its own single-view call (each work item
+    runs the same arithmetic either way)."""
+    W = 4
+    wl = workloads.make_workload("views", [700, 90, 1500, 33], [4, 3, 8, 2], 16, 16,
+                                 world_size=W, num_segments=S, seed=11)
+    step = runner.step_for_workload(wl, "cuda")
+    q, kv, seq, ind, bt = runner.device_inputs(wl, "cuda")
+    step(q, kv, seq, ind, bt, wl.sm_scale)  # fills the row views and sub-page tables
+    torch.cuda.synchronize()
+    all_out, all_lse, _ = mla.decode_verify(q, kv, ind, step.row_len_local, step.subpage, step.P, S,
+                                            int(wl.qlens.max()), wl.sm_scale, num_views=W)
+    for r in range(W):
+        o, l, _ = mla.decode_verify(q, kv, ind, step.row_len_local[r], step.subpage[r], step.P, S,
+                                    int(wl.qlens.max()), wl.sm_scale)
+        torch.cuda.synchronize()
+        assert torch.equal(o, all_out[r]) and torch.equal(l, all_lse[r]), f"view {r}"
+    assert mla.get_device_error() == 0
 
 
 def test_many_rows_per_request_and_short_windows():
