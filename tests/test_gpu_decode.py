@@ -64,6 +64,18 @@ def test_block_sizes_and_subpages(block_size):
     _full_check(wl, f"block_size {block_size}")
 
 
+@pytest.mark.parametrize("block_size", [16, 256])
+def test_fp8_block_sizes_every_pair(block_size):
+    """fp8 through both load paths: 16-row pages (one 2-D box per chunk and
+    page, packed into the stage's upper half) and 128-row sub-pages (one 3-D
+    box per 64-token tile, a sub-page spanning two tiles)."""
+    rng = np.random.default_rng(300 + block_size)
+    L = rng.integers(5, 1200, 5)
+    wl = workloads.make_workload(f"fp8_bs{block_size}", L, np.minimum(L, 3), 12, block_size,
+                                 kv_dtype="fp8", num_segments=2, seed=block_size)
+    _full_check(wl, f"fp8 block_size {block_size}")
+
+
 @pytest.mark.parametrize("W,I", [(8, 4), (3, 16), (2, 64)])
 def test_dcp_interleaved_every_pair(W, I):
     """Interleave I > 1 (runs of I positions dealt to the shards in turn):
