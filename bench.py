@@ -434,9 +434,10 @@ def main():
         try:
             with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
                 tr = json.load(f)
-            if tr.get("kernel_source_sha256") == source_hash() and tr.get("workload") == wl.name:
-                traffic = tr.get("bytes_per_launch")
-        except (OSError, ValueError):
+            for ent in tr.get("entries", [tr]):
+                if ent.get("kernel_source_sha256") == source_hash() and ent.get("workload") == wl.name:
+                    traffic = ent.get("bytes_per_launch")
+        except (OSError, ValueError, AttributeError):
             pass
         roofline = {"kernel": "mla_decode_kernel<bf16>" if wl.kv_dtype == "bf16" else
                     "mla_decode_kernel<fp8>", "bound": "hbm", "achieved": achieved,
