@@ -11,30 +11,34 @@
 // natural-log LSE directly.
 //
 // GB300 design (not the pages' ROCm design):
-//  * Work item = (request, block of <= 64 query rows, split-K segment).  The
-//    rows of a request (heads x qlen) are decoded jointly against shared
-//    64-token KV tiles, so each latent row is read from HBM once per request
-//    (the pages replicate the request once per verify row).
+//  * Work item = (request, row view, block of <= 64 query rows, split-K
+//    segment).  The rows of a request (heads x qlen) are decoded jointly
+//    against shared 64-token KV tiles, so each latent row is read from HBM
+//    once per request (the pages replicate the request once per verify row);
+//    several row views of the same queries (the shard views of a DCP step)
+//    can share one launch.
 //  * Persistent CTAs, one per SM.  The producer warp claims items from an
-//    atomic counter (dynamic load balance) and publishes each decoded item,
-//    with its rows' visible lengths, through a 4-deep shared-memory work
-//    ring.  Every barrier phase follows one running tile counter.
+//    atomic counter (dynamic load balance, longest requests first) and
+//    publishes each decoded item, with its rows' visible lengths, through a
+//    4-deep shared-memory work ring.  Every barrier phase follows one running
+//    tile counter.
 //  * Swapped operand order, so the output accumulator fits TMEM densely:
 //        S^T[64 tok, 64 rows]     = K_tile[64, 576] . Q[64, 576]^T      (M = 64, K-major A and B)
 //        O^T[4x128 dims, 64 rows] += V^T[512, 64 tok] . P^T[64, 64]^T   (M = 128, MN-major A and B)
 //    TMEM: O^T in columns 0-255 (4 blocks x 64), S^T of stage s in columns
 //    256 + 64 s (an M = 64 result puts token 16 q + i in lane 32 q + i).
 //  * Two shared-memory stages of one 64-token tile each: nine 8 KB chunks of
-//    64 tokens x 64 dims (128-byte swizzle), the eight V chunks adjacent so
-//    PV reads them in place, the rope chunk last; once QK has retired a
-//    stage's rope chunk it receives that tile's P^T.  The UMMA warp issues
-//    QK of tile i + 1 before PV of tile i, so the loads of one stage and the
-//    QK of the next overlap the softmax of the current tile.  Q (64 x 576)
-//    is resident per item.
+//    64 tokens x 64 dims (128-byte swizzle; one 3-D TMA box per tile when the
+//    page size is >= 64), the eight V chunks adjacent so PV reads them in
+//    place, the rope chunk last; once QK has retired a stage's rope chunk it
+//    receives that tile's P^T.  Q (64 x 576) is resident per item.
+//  * The UMMA warp runs an event loop over non-blocking barrier tests: a PV
+//    whose P^T is ready goes first (it frees a stage for the next load), QK of
+//    the next tile runs while the softmax of the current one is under way.
 //  * Warp roles: warps 0-7 softmax (column group g = warp / 4 owns rows
 //    32g..32g+31; TMEM lane quarter = warp % 4), warp 8 TMA producer, warp 9
-//    UMMA issuer and TMEM owner.  fp8 tiles are TMA-loaded into the upper
-//    half of each chunk and expanded in place to bf16 by the softmax warps.
+//    UMMA issuer and TMEM owner.  fp8 tiles are TMA-loaded packed into the
+//    stage's upper half and expanded in place to bf16 by the softmax warps.
 //  * Lazy rescaling: the running reference max only moves when a tile's max
 //    exceeds it by more than 2^8, so O is rarely rescaled in TMEM.
 //  * Every wait is bounded; a timeout records MLA_DEV_WAIT_TIMEOUT, lets all
