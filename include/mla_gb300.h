@@ -52,7 +52,7 @@ typedef struct CUstream_st *mla_stream_t;
 
 #define MLA_D_QK 576  /* q / K width: 512 latent + 64 rope   */
 #define MLA_D_V 512   /* V / output width: the 512-d latent */
-#define MLA_ABI_VERSION 2
+#define MLA_ABI_VERSION 3
 
 typedef enum mla_status {
   MLA_OK = 0,
@@ -182,10 +182,11 @@ typedef enum mla_decode_flags {
 
 /* Workspace bytes mla_decode_verify needs for `a`.  Layout, each region
  * starting on a 256-byte boundary, in this order:
- *   segm_out [V, B, RB, S, 512, 64] bf16: RB = ceil(max_qlen * H / 64) row
- *     blocks per request; block (v, b, rb, s) holds, dim-major (64 rows
- *     innermost), segment s of view v's rows rb*64 .. rb*64 + 63 of request b,
- *     a request's rows numbered t * H + h; rows past qlen * H are unused;
+ *   segm_out [V, B, RB, S, 8, 512, 8] bf16: RB = ceil(max_qlen * H / 64) row
+ *     blocks per request; block (v, b, rb, s) holds segment s of view v's
+ *     rows rb*64 .. rb*64 + 63 of request b (a request's rows numbered
+ *     t * H + h) as [row octet][dim][row within the octet]: block row i, dim d
+ *     at ((i / 8) * 512 + d) * 8 + i % 8; rows past qlen * H are unused;
  *   segm_max [V, T, H, S] float32, segm_sum [V, T, H, S] float32
  *   (these three only when num_segments > 1), then 256 bytes of scheduler
  *   state (a work counter the call zeroes on the stream before its kernel).
@@ -230,7 +231,7 @@ typedef struct mla_merge_args {
   int num_heads;   /* H */
   int num_parts;   /* S segments or W shards, 1 <= num_parts <= 1024 */
   /* MLA_MERGE_SEGMENTS: the decode workspace's partials: segm_out
-   * [B, RB, S, 512, 64] bf16 unnormalised outputs (uint16 bit patterns; the
+   * [B, RB, S, 8, 512, 8] bf16 unnormalised outputs (uint16 bit patterns; the
    * block layout of mla_decode_verify_workspace), segm_max / segm_sum
    * [T, H, S] float32 base-2 maxima and exp2 sums.  A part with max = -inf
    * is empty and contributes nothing (its output is not read as a value). */

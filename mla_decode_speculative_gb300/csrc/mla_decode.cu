@@ -824,20 +824,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&misc.p_full[st]));
       }
 
-      // ---- epilogue of the item: row sums, statistics, output
-      if (ok && !mbar_wait(smem_u32(&misc.o_done[(g - 1) & 1u]), ((g - 1) >> 1) & 1u, abort_flag, budget)) {
-        fail();
-        ok = false;
-      }
-      tc_fence_after();
+      // ---- epilogue of the item: row sums and statistics (while the last
+      // PV runs), then the output
       const float wsum = half_reduce_scatter<false>(l_part, lane);  // column `lane` of the group
       misc.red[red_buf][g_col][wq][lane] = wsum;
       named_bar_sync(1 + g_col, 128);
       const float l_tot = misc.red[red_buf][g_col][0][lane] + misc.red[red_buf][g_col][1][lane] +
                           misc.red[red_buf][g_col][2][lane] + misc.red[red_buf][g_col][3][lane];
       red_buf ^= 1;
-      const bool write = ok && (*abort_flag == 0);
-      if (write && wq == 0 && my_col < n_rows) {
+      if (ok && wq == 0 && my_col < n_rows) {
         const int64_t r = row_base + my_col;
         if (direct) {
           p.lse[r] = (l_tot > 0.0f) ? (m_ref + __log2f(l_tot)) * kLn2 : -INFINITY;
@@ -853,6 +848,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) sc[j] = __shfl_sync(0xffffffffu, col_scale, j);
       const int64_t r0 = row_base + 32 * g_col;
+      if (ok && !mbar_wait(smem_u32(&misc.o_done[(g - 1) & 1u]), ((g - 1) >> 1) & 1u, abort_flag, budget)) {
+        fail();
+        ok = false;
+      }
+      tc_fence_after();
       // O^T blocks two at a time: both TMEM loads in flight, one wait
 #pragma unroll 1
       for (int b2 = 0; b2 < 4; b2 += 2) {
@@ -864,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h2 = 0; h2 < 2; ++h2) {
           const int blk = b2 + h2;
           const uint32_t (&ov)[32] = ovp[h2];
-          if (!write) continue;
+          if (!ok || *abort_flag != 0) continue;
           const int dim = blk * 128 + dim_lane;
           if (direct) {
             __nv_bfloat16 *o = p.out + r0 * 512 + dim;
@@ -872,12 +872,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 32; ++j)
               if (j < n_cols) o[static_cast<int64_t>(j) * 512] = __float2bfloat16_rn(__uint_as_float(ov[j]) * sc[j]);
           } else {
-            // partial block (b, rb, seg), dim-major [512][64]: this thread's
-            // dim, the group's 32 rows as four 16-byte stores (a row that saw
-            // no token here gets 0)
+            // partial block (b, rb, seg), [8 row octets][512 dims][8 rows]:
+            // this thread's dim in the group's four octets, one 16-byte store
+            // each; a warp's store covers 32 consecutive dims, 512 contiguous
+            // bytes (a row that saw no token here gets 0)
             uint4 *o = reinterpret_cast<uint4 *>(
-                p.segm_out + ((static_cast<int64_t>(e_b) * p.row_blocks + e_rb) * S + seg) * (512 * kRows) +
-                dim * kRows + 32 * g_col);
+                           p.segm_out + ((static_cast<int64_t>(e_b) * p.row_blocks + e_rb) * S + seg) * (512 * kRows)) +
+                       (4 * g_col) * 512 + dim;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint32_t w4[4];
@@ -888,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float hi = sc[j + 1] != 0.0f ? __uint_as_float(ov[j + 1]) * sc[j + 1] : 0.0f;
                 w4[u] = pack_bf16(lo, hi);
               }
-              o[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              o[q * 512] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
           }
         }

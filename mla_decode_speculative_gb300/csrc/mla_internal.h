@@ -65,7 +65,7 @@ struct MergeLaunch {
   int num_rows;
   int num_heads;
   int num_parts;
-  const uint16_t *segm_out;  // bf16 blocks [B, RB, S, 512, 64]
+  const uint16_t *segm_out;  // bf16 blocks [B, RB, S, 8, 512, 8]
   const float *segm_max;
   const float *segm_sum;
   const int32_t *qo_indptr;  // segment mode

@@ -14,11 +14,13 @@
 // gives out = 0, lse = -inf.
 //
 // Segment partials come in the decode kernel's block layout: per (request,
-// 64-row block, segment) a dim-major [512][64] bf16 block.  One CTA merges
-// 64 output dims of one row block: lane l owns rows 2l and 2l+1, warp w dims
-// 8w..8w+7 of the CTA's 64, so every segment costs a warp eight coalesced
-// 128-byte loads (four segments in flight), with per-row weights staged in
-// shared memory; each thread writes one 16-byte piece of two rows.
+// 64-row block, segment) a bf16 block [8 row octets][512 dims][8 rows].  One
+// CTA merges 64 output dims of one row block: warp w takes dims 8w..8w+7 of
+// the CTA's 64, lane l the rows of octet l/4 for two of those dims, so every
+// segment costs a warp two 16-byte loads per lane over eight 128-byte runs
+// (four segments in flight), with per-row weights staged in shared memory;
+// the merged 64 x 64 tile is transposed in shared memory and written as
+// 128-byte row pieces.
 // State partials are row-major [W][T*H][512] bf16: one 128-thread block per
 // (row, head), thread t owning dims 4t..4t+3.  Both are HBM/L2 streaming
 // reductions.
@@ -48,7 +50,7 @@ struct StateParams {
 };
 
 struct SegParams {
-  const __nv_bfloat16 *segm_out;  // [B, RB, S, 512, 64]
+  const __nv_bfloat16 *segm_out;  // [B, RB, S, 8, 512, 8]
   const float *segm_max;          // [T*H, S]
   const float *segm_sum;
   const int32_t *qo_indptr;
@@ -86,7 +88,8 @@ constexpr int kSegChunk = 32;  // segments whose weights are staged at a time
 // 2^(m_s - M) / den for 32 segments at a time, in shared memory, and streams
 // the partial blocks four segments deep.
 __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
-  __shared__ float s_w[kSegChunk][kBlockRows];
+  __shared__ __align__(16) float s_w[kSegChunk][kBlockRows];
+  __shared__ __align__(16) uint32_t s_o[kBlockRows][kDimsPerCta / 2 + 4];  // bf16 pairs, padded rows
   __shared__ int s_live[kSegChunk];
   __shared__ float s_part[4][kBlockRows];
   __shared__ float s_M[kBlockRows], s_inv[kBlockRows];
@@ -131,8 +134,9 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
   __syncthreads();
 
   const int dim0 = blockIdx.y * kDimsPerCta + warp * 8;
-  const int r0 = 2 * lane, r1 = 2 * lane + 1;  // this lane's rows of the block
-  float a0[8], a1[8];
+  const int oct = lane >> 2;          // rows 8 oct .. 8 oct + 7 of the block
+  const int dp = 2 * (lane & 3);      // dims dim0 + dp, dim0 + dp + 1
+  float a0[8], a1[8];                 // [row of the octet] for the two dims
 #pragma unroll
   for (int k = 0; k < 8; ++k) a0[k] = a1[k] = 0.0f;
   const int64_t blk0 = (static_cast<int64_t>(vb) * p.row_blocks + rb) * S;
@@ -153,42 +157,53 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
     }
     __syncthreads();
     for (int sc0 = 0; sc0 < nc; sc0 += 4) {
-      uint32_t x[4][8];
-      float w0[4], w1[4];
+      uint4 x[4][2];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int sc = sc0 + u;
-        const bool live = sc < nc && s_live[sc];
-        w0[u] = live ? s_w[sc][r0] : 0.0f;
-        w1[u] = live ? s_w[sc][r1] : 0.0f;
-        if (live) {
-          const uint32_t *src = reinterpret_cast<const uint32_t *>(
-              p.segm_out + ((blk0 + c0 + sc) * 512 + dim0) * kBlockRows) + lane;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) x[u][k] = __ldcs(src + k * (kBlockRows / 2));
+        if (sc < nc && s_live[sc]) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + c0 + sc) * (512 * kBlockRows)) +
+                             oct * 512 + dim0 + dp;
+          x[u][0] = __ldcs(src);
+          x[u][1] = __ldcs(src + 1);
         } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) x[u][k] = 0u;
+          x[u][0] = x[u][1] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
       // a weight of 0 selects 0: an empty row's slot is never used as a value
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 4; ++u) {
+        const int sc = sc0 + u;
+        if (sc >= nc || !s_live[sc]) continue;
+        const float4 wa = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oct]);
+        const float4 wb = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oct + 4]);
+        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        const uint32_t v0[4] = {x[u][0].x, x[u][0].y, x[u][0].z, x[u][0].w};
+        const uint32_t v1[4] = {x[u][1].x, x[u][1].y, x[u][1].z, x[u][1].w};
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          a0[k] += (w0[u] != 0.0f) ? w0[u] * bf16_lo(x[u][k]) : 0.0f;
-          a1[k] += (w1[u] != 0.0f) ? w1[u] * bf16_hi(x[u][k]) : 0.0f;
+          const float e0 = (k & 1) ? bf16_hi(v0[k >> 1]) : bf16_lo(v0[k >> 1]);
+          const float e1 = (k & 1) ? bf16_hi(v1[k >> 1]) : bf16_lo(v1[k >> 1]);
+          a0[k] += (w[k] != 0.0f) ? w[k] * e0 : 0.0f;
+          a1[k] += (w[k] != 0.0f) ? w[k] * e1 : 0.0f;
         }
+      }
     }
     __syncthreads();  // s_w / s_live are refilled by the next chunk
   }
-  const int64_t g0 = grow0 + r0;
-  if (r0 < n_rows)
-    *reinterpret_cast<uint4 *>(p.out + g0 * 512 + dim0) =
-        make_uint4(pack_bf16(a0[0], a0[1]), pack_bf16(a0[2], a0[3]), pack_bf16(a0[4], a0[5]), pack_bf16(a0[6], a0[7]));
-  if (r1 < n_rows)
-    *reinterpret_cast<uint4 *>(p.out + (g0 + 1) * 512 + dim0) =
-        make_uint4(pack_bf16(a1[0], a1[1]), pack_bf16(a1[2], a1[3]), pack_bf16(a1[4], a1[5]), pack_bf16(a1[6], a1[7]));
+  // transpose through shared memory: row 8 oct + k, dims (warp * 8 + dp, +1)
+#pragma unroll
+  for (int k = 0; k < 8; ++k) s_o[8 * oct + k][warp * 4 + (lane & 3)] = pack_bf16(a0[k], a1[k]);
+  __syncthreads();
+  // 64 rows x 128 bytes: thread t writes 16-byte pieces t and t + 256
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = tid + 256 * h, r = i >> 3, c16 = i & 7;
+    if (r < n_rows) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(&s_o[r][4 * c16]);
+      *reinterpret_cast<uint4 *>(p.out + (grow0 + r) * 512 + blockIdx.y * kDimsPerCta + 8 * c16) = v;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- states

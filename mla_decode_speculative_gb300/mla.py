@@ -292,8 +292,9 @@ def row_blocks(max_qlen: int, num_heads: int) -> int:
 
 def workspace_views(workspace: torch.Tensor, num_reqs: int, max_qlen: int, num_rows: int,
                     num_heads: int, num_segments: int, num_views: int = 1):
-    """The documented workspace layout (num_views = 1): (segm_out [B, RB, S, 512, 64] bf16
-    blocks, segm_max [T, H, S], segm_sum [T, H, S]); V views stack V such layouts."""
+    """The documented workspace layout (num_views = 1): (segm_out [B, RB, S, 8, 512, 8] bf16
+    blocks -- row octet, dim, row in octet --, segm_max [T, H, S], segm_sum [T, H, S]); V
+    views stack V such layouts."""
     num_reqs, num_rows = num_reqs * num_views, num_rows * num_views
     items = num_rows * num_heads * num_segments
     blocks = num_reqs * row_blocks(max_qlen, num_heads) * num_segments
@@ -301,7 +302,7 @@ def workspace_views(workspace: torch.Tensor, num_reqs: int, max_qlen: int, num_r
     o_bytes = a256(blocks * 512 * 64 * 2)
     m_bytes = a256(items * 4)
     segm_out = workspace[:blocks * 512 * 64 * 2].view(torch.bfloat16).view(
-        num_reqs, row_blocks(max_qlen, num_heads), num_segments, 512, 64)
+        num_reqs, row_blocks(max_qlen, num_heads), num_segments, 8, 512, 8)
     segm_max = workspace[o_bytes:o_bytes + items * 4].view(torch.float32).view(num_rows, num_heads, num_segments)
     segm_sum = workspace[o_bytes + m_bytes:o_bytes + m_bytes + items * 4].view(torch.float32).view(
         num_rows, num_heads, num_segments)
@@ -310,7 +311,7 @@ def workspace_views(workspace: torch.Tensor, num_reqs: int, max_qlen: int, num_r
 
 def merge_segments(segm_out, segm_max, segm_sum, qo_indptr, max_qlen, out=None, lse=None,
                    stream=None):
-    """mla_merge_segments, segment mode: bf16 partial blocks [B, RB, S, 512, 64] (the
+    """mla_merge_segments, segment mode: bf16 partial blocks [B, RB, S, 8, 512, 8] (the
     decode workspace layout) + [T, H, S] f32 base-2 stats; qo_indptr [B + 1] int32."""
     T, H, S = segm_max.shape
     if out is None:

@@ -78,25 +78,26 @@ def run_gpu(wl, num_segments=None, device="cuda"):
 
 def rows_to_blocks(x, qo_indptr, num_heads, row_blocks):
     """[T, H, S, 512] per-(row, head) partials -> the decode workspace's block
-    layout [B, RB, S, 512, 64] (a request's rows t * H + h, 64 per block,
-    dim-major; unused rows left as NaN so that reading one would show)."""
+    layout [B, RB, S, 8, 512, 8] (a request's rows t * H + h, 64 per block;
+    block row i sits in row octet i // 8 at position i % 8 of each dim; unused
+    rows left as NaN so that reading one would show)."""
     T, H, S, D = x.shape
     B = len(qo_indptr) - 1
-    out = np.full((B, row_blocks, S, D, 64), np.nan, dtype=x.dtype)
+    out = np.full((B, row_blocks, S, 8, D, 8), np.nan, dtype=x.dtype)
     flat = x.reshape(T * H, S, D)
     for b in range(B):
         r0, r1 = int(qo_indptr[b]) * H, int(qo_indptr[b + 1]) * H
         for i in range(r1 - r0):
-            out[b, i // 64, :, :, i % 64] = flat[r0 + i]
+            out[b, i // 64, :, (i % 64) // 8, :, i % 8] = flat[r0 + i]
     return out
 
 
 def blocks_to_rows(blocks, qo_indptr, num_heads, num_rows):
-    """Inverse of rows_to_blocks: [B, RB, S, 512, 64] -> [T, H, S, 512]."""
-    B, RB, S, D, _ = blocks.shape
+    """Inverse of rows_to_blocks: [B, RB, S, 8, 512, 8] -> [T, H, S, 512]."""
+    B, RB, S, _, D, _ = blocks.shape
     out = np.zeros((num_rows * num_heads, S, D), dtype=blocks.dtype)
     for b in range(B):
         r0, r1 = int(qo_indptr[b]) * num_heads, int(qo_indptr[b + 1]) * num_heads
         for i in range(r1 - r0):
-            out[r0 + i] = blocks[b, i // 64, :, :, i % 64]
+            out[r0 + i] = blocks[b, i // 64, :, (i % 64) // 8, :, i % 8]
     return out.reshape(num_rows, num_heads, S, D)
