@@ -52,7 +52,7 @@ typedef struct CUstream_st *mla_stream_t;
 
 #define MLA_D_QK 576  /* q / K width: 512 latent + 64 rope   */
 #define MLA_D_V 512   /* V / output width: the 512-d latent */
-#define MLA_ABI_VERSION 3
+#define MLA_ABI_VERSION 4
 
 typedef enum mla_status {
   MLA_OK = 0,
@@ -158,7 +158,8 @@ typedef struct mla_decode_args {
   const int32_t *subpage_table;  /* [B, subpage_stride] sub-page ids (mla_plan_rows) */
   int subpage_stride;
   int page_size;         /* P = mla_page_size(block_size); 8 <= P <= 128 */
-  int num_segments;      /* S split-K segments per request, 1 <= S <= 1024 */
+  int num_segments;      /* S: split-K segment slots per (view, request, row
+                          * block), 1 <= S <= 1024 -- see mla_decode_flags */
   void *out;             /* [T, H, 512] bf16 output */
   float *lse;            /* [T, H] natural-log LSE (-inf for a row with no tokens) */
   int flags;             /* bitwise OR of mla_decode_flags (0 = default) */
@@ -177,7 +178,20 @@ typedef enum mla_decode_flags {
    * partials in the workspace (layout of mla_decode_verify_workspace) for the
    * caller's own mla_merge_segments call; out / lse are not written.  This is
    * the pages' two-step form (segmented decode, then merge_mla_segments). */
-  MLA_DECODE_SKIP_MERGE = 1
+  MLA_DECODE_SKIP_MERGE = 1,
+  /* How the S > 1 segment slots are filled.  Default (flag clear, and at most
+   * 1024 (view, request, row block) units): balanced split -- the units'
+   * 64-token KV tiles, laid end to end in unit order, are cut into equal
+   * contiguous chunks, one per SM (grown where needed so that no unit meets
+   * more than S chunks); the part of a unit inside chunk c is its segment
+   * c - c0 (c0: the unit's first chunk), and slots past a unit's last part
+   * hold max = -inf, sum = 0.  Every SM then streams the same number of
+   * tiles, whatever the mix of lengths.  With this flag (or more units): the
+   * pages' split [vLLM #51705, 实现拆解 4] -- segment s of a request holds
+   * tokens [s*L, (s+1)*L) with L = ceil(len / (S*P)) * P, len the
+   * request's longest visible row.  The merged out / lse are the same either
+   * way up to float rounding. */
+  MLA_DECODE_UNIFORM_SEGMENTS = 2
 } mla_decode_flags;
 
 /* Workspace bytes mla_decode_verify needs for `a`.  Layout, each region

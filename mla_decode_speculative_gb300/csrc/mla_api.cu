@@ -443,7 +443,7 @@ static mla_status check_decode_args(const mla_decode_args *a) {
     set_error("mla_decode_verify: num_views %d (rows x heads x views must fit int32)", a->num_views);
     return MLA_ERR_INVALID_ARG;
   }
-  if ((a->flags & ~MLA_DECODE_SKIP_MERGE) != 0) {
+  if ((a->flags & ~(MLA_DECODE_SKIP_MERGE | MLA_DECODE_UNIFORM_SEGMENTS)) != 0) {
     set_error("mla_decode_verify: unknown flags 0x%x", a->flags);
     return MLA_ERR_INVALID_ARG;
   }

@@ -84,12 +84,14 @@ constexpr int kOffMisc = kOffQ + kNumChunks * kQChunkBytes;
 
 // One claimed work item as published by the producer to the other roles.
 struct WorkEntry {
-  int w;          // item index, -1 = no more work
+  int w;          // claim index (item or chunk), -1 = no more work
   int b, rb, seg, q_row, row_base, n_rows, seg_lo, seg_hi, n_tiles;  // b: view * B + request
+  int fill_hi;    // segment slots seg+1 .. fill_hi-1 of these rows get no part: mark them empty
   alignas(16) int lens[kRows];  // visible tokens of each of the block's rows (0 past n_rows)
 };
 constexpr int kWorkRing = 4;
 constexpr int kMaxOrderedReqs = 128;  // requests ranked longest-first in every CTA
+constexpr int kMaxUnits = 1024;       // balanced split: (view, request, row block) units tabulated per CTA
 
 struct Misc {
   uint64_t full[kStages];
@@ -106,6 +108,7 @@ struct Misc {
   int sm_stop[2];  // softmax warps' shared exit decision (double-buffered)
   int req_key[kMaxOrderedReqs];   // a request's longest row (producer's scratch)
   int req_order[kMaxOrderedReqs]; // requests, longest first
+  int unit_end[kMaxUnits];        // balanced split: tiles of units 0..u (inclusive prefix sum)
   float red[2][2][4][32];  // [buffer][column group][lane quarter][lane]
 };
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc)) + 1024;
@@ -137,6 +140,8 @@ struct Params {
   int num_rows;
   int max_len;
   int tile3d;              // KV tensor map is the 3-D whole-tile view (page size >= 64)
+  int balanced;            // split-K by equal chunks of the batch's tiles (else S equal segments per request)
+  int num_units;           // num_views * num_reqs * row_blocks
   float score_scale_log2;  // sm_scale * kv_scale * log2(e)
   float out_scale;         // kv_scale (fp8) or 1
 };
@@ -151,20 +156,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Decodes item w into a work entry (the whole producer warp): request, row
-// block, segment range, and the visible length of each row of the block.
-// Returns false when the request's qo_indptr is inconsistent (the item is
-// then published with no rows).  Requests with more than 32 verify rows read
-// the extra lengths directly.
-__device__ __forceinline__ bool decode_item(const Params &p, int w, WorkEntry &e, int lane,
-                                            bool &clipped, const int *order) {
-  const int S = p.num_segments;
-  const int seg = w % S;
-  const int rb = (w / S) % p.row_blocks;
-  // item order: request (longest first), then view, row block, segment
-  const int v = (w / (S * p.row_blocks)) % p.num_views;
-  const int ob = w / (S * p.row_blocks * p.num_views);
-  const int b = order != nullptr ? order[ob] : ob;
+// Fills the request / row-block part of a work entry (the whole producer
+// warp): rows of the block and the visible length of each, and returns the
+// request's longest visible length (every row clamped to [0, max_len]) in
+// group_len.  Returns false when the request's qo_indptr is inconsistent (the
+// entry then has no rows).  Requests with more than 32 verify rows read the
+// extra lengths directly.
+__device__ __forceinline__ bool decode_unit(const Params &p, int v, int b, int rb, WorkEntry &e, int lane,
+                                            bool &clipped, int &group_len) {
   const int vrow = v * p.num_rows;  // view v's rows start here in row_len / out / lse
   const int q0 = p.qo_indptr[b];
   const int q1 = p.qo_indptr[b + 1];
@@ -177,7 +176,7 @@ __device__ __forceinline__ bool decode_item(const Params &p, int w, WorkEntry &e
   // lengths of the request's rows: lane t holds row t (t < 32)
   int my_len = 0;
   if (lane < qlen) my_len = p.row_len[vrow + q0 + lane];
-  int group_len = 0;
+  group_len = 0;
   for (int t = lane; t < qlen; t += 32) {
     int l = t == lane ? my_len : p.row_len[vrow + q0 + t];
     if (l > p.max_len) { clipped = true; l = p.max_len; }
@@ -197,20 +196,23 @@ __device__ __forceinline__ bool decode_item(const Params &p, int w, WorkEntry &e
     e.lens[c] = c < n_rows ? min(max(l, 0), p.max_len) : 0;
   }
   if (lane == 0) {
-    const long long span = static_cast<long long>(S) * p.page_size;
-    const int seg_tokens = static_cast<int>((group_len + span - 1) / span) * p.page_size;
-    e.w = w;
     e.b = v * p.num_reqs + b;
     e.rb = rb;
-    e.seg = seg;
     e.q_row = q0 * p.num_heads + row_begin;
     e.n_rows = n_rows;
     e.row_base = (vrow + q0) * p.num_heads + row_begin;
-    e.seg_lo = seg * seg_tokens;
-    e.seg_hi = min(e.seg_lo + seg_tokens, group_len);
-    e.n_tiles = (n_rows > 0 && e.seg_lo < e.seg_hi) ? (e.seg_hi - e.seg_lo + kTileTok - 1) / kTileTok : 0;
   }
   return ok;
+}
+
+// The same longest visible length, by one thread (the balanced split's unit
+// table); 0 for an inconsistent qo_indptr.
+__device__ __forceinline__ int request_len(const Params &p, int v, int b) {
+  const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
+  if (q0 < 0 || q1 < q0 || q1 > p.num_rows || q1 - q0 > p.max_qlen) return 0;
+  int len = 0;
+  for (int t = q0; t < q1; ++t) len = max(len, min(max(p.row_len[v * p.num_rows + t], 0), p.max_len));
+  return len;
 }
 
 // Warp transpose-reduce: on entry v[k] is this lane's value of column k; on
@@ -318,6 +320,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc.abort = 0;
     fence_mbar_init();
   }
+  const bool balanced = p.balanced != 0;
+  if (balanced) {
+    // tiles of every (view, request, row block) unit: the request's longest
+    // visible length in 64-token tiles, 0 for a row block without rows
+    const int n_vb = p.num_views * p.num_reqs;
+    for (int vb = threadIdx.x; vb < n_vb; vb += kThreads) {
+      const int v = vb / p.num_reqs, b = vb % p.num_reqs;
+      const int len = request_len(p, v, b);
+      const int rows = len > 0 ? (p.qo_indptr[b + 1] - p.qo_indptr[b]) * p.num_heads : 0;
+      const int t = (len + kTileTok - 1) / kTileTok;
+      for (int rb = 0; rb < p.row_blocks; ++rb) misc.unit_end[vb * p.row_blocks + rb] = rb * kRows < rows ? t : 0;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -356,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // by their longest row (a request's rows are nondecreasing, so its last
     // row), ties by index, and claims in that order.
     const int *order = nullptr;
-    if (p.num_reqs <= kMaxOrderedReqs) {
+    if (!balanced && p.num_reqs <= kMaxOrderedReqs) {
       for (int b = lane; b < p.num_reqs; b += 32) {
         const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
         misc.req_key[b] = (q0 >= 0 && q1 > q0 && q1 <= p.num_rows) ? p.row_len[q1 - 1] : 0;
@@ -374,6 +389,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       order = misc.req_order;
     }
+    // Balanced split: the units' T tiles laid end to end are cut into n
+    // chunks, chunk c = [floor(c T / n), floor((c+1) T / n)), one per CTA
+    // (n smaller when that keeps every unit within S chunks); a chunk's part
+    // of each unit it meets is one segment of that unit, numbered by chunk
+    // from the unit's first.
+    const int n_units = p.num_units;
+    int T = 0, n_chunks = 0;
+    if (balanced) {
+      int carry = 0, tmax = 0;
+      for (int base = 0; base < n_units; base += 32) {  // inclusive prefix sum, in place
+        const int u = base + lane;
+        int x = u < n_units ? misc.unit_end[u] : 0;
+        tmax = max(tmax, x);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (u < n_units) misc.unit_end[u] = carry + x;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+      __syncwarp();
+      T = carry;
+      // chunks of at least `need` tiles meet at most S chunks per unit (S >= 2 here)
+      const int need = max((tmax + S - 2) / (S - 1), 1);
+      n_chunks = T > 0 ? min(static_cast<int>(gridDim.x), max(T / need, 1)) : 1;
+    }
+    // chunk holding tile x (T > 0)
+    auto chunk_of = [&](int x) {
+      return static_cast<int>((static_cast<long long>(x + 1) * n_chunks - 1) / T);
+    };
+    int chunk = -1, c_lo = 0, c_hi = 0, c_hi_ext = 0, u_next = 0;
     for (uint32_t k = 0;; ++k) {
       const uint32_t ws = k % kWorkRing;
       WorkEntry &e = misc.work[ws];
@@ -383,10 +432,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      int w = 0;
-      if (lane == 0) w = ok ? atomicAdd(p.sched, 1) : p.num_items;
-      w = __shfl_sync(0xffffffffu, w, 0);
-      if (w >= p.num_items) {
+      // the next part: (view, request, row block), segment slot, tile range
+      bool done = !ok;
+      int w = 0, v = 0, b = 0, rb = 0, seg = 0, fill_hi = 0, t_a = 0, t_b = 0, u_start = 0;
+      if (!done && balanced) {
+        while (true) {
+          if (chunk < 0) {
+            int c = 0;
+            if (lane == 0) c = atomicAdd(p.sched, 1);
+            c = __shfl_sync(0xffffffffu, c, 0);
+            if (c >= n_chunks) {
+              done = true;
+              break;
+            }
+            chunk = c;
+            c_lo = static_cast<int>(static_cast<long long>(c) * T / n_chunks);
+            c_hi = static_cast<int>(static_cast<long long>(c + 1) * T / n_chunks);
+            c_hi_ext = c == n_chunks - 1 ? T + 1 : c_hi;  // units without tiles at the very end
+            int u = 0, u_hi = n_units;  // first unit whose prefix reaches c_lo
+            while (u < u_hi) {
+              const int mid = (u + u_hi) >> 1;
+              if (misc.unit_end[mid] < c_lo) u = mid + 1;
+              else u_hi = mid;
+            }
+            u_next = u;
+          }
+          bool found = false;
+          while (u_next < n_units) {
+            const int u = u_next;
+            const int end = misc.unit_end[u];
+            const int start = u == 0 ? 0 : misc.unit_end[u - 1];
+            if (start >= c_hi_ext) break;
+            ++u_next;
+            if (end > start && end <= c_lo) continue;  // all of its tiles lie before this chunk
+            if (end == start) {  // no tiles: one empty part marks all its slots
+              t_a = t_b = start;
+              seg = 0;
+              fill_hi = S;
+            } else {
+              t_a = max(c_lo, start);
+              t_b = min(c_hi, end);
+              seg = chunk - chunk_of(start);
+              fill_hi = end <= c_hi ? S : seg + 1;  // its last part marks the slots no chunk reached
+            }
+            u_start = start;
+            const int vb = u / p.row_blocks;
+            rb = u - vb * p.row_blocks;
+            v = vb / p.num_reqs;
+            b = vb - v * p.num_reqs;
+            found = true;
+            break;
+          }
+          if (found) break;
+          chunk = -1;  // chunk exhausted: claim the next
+        }
+        w = chunk;
+      } else if (!done) {
+        if (lane == 0) w = atomicAdd(p.sched, 1);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (w >= p.num_items) {
+          done = true;
+        } else {
+          // item order: request (longest first), then view, row block, segment
+          seg = w % S;
+          fill_hi = seg + 1;
+          rb = (w / S) % p.row_blocks;
+          v = (w / (S * p.row_blocks)) % p.num_views;
+          const int ob = w / (S * p.row_blocks * p.num_views);
+          b = order != nullptr ? order[ob] : ob;
+        }
+      }
+      if (done) {
         if (lane == 0) {
           e.w = -1;
           mbar_arrive(smem_u32(&misc.work_full[ws]));
@@ -394,9 +510,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       bool clipped = false;
-      const bool good = decode_item(p, w, e, lane, clipped, order);
+      int group_len = 0;
+      const bool good = decode_unit(p, v, b, rb, e, lane, clipped, group_len);
       __syncwarp();
       if (lane == 0) {
+        e.w = w;
+        e.seg = seg;
+        e.fill_hi = fill_hi;
+        if (balanced) {
+          e.seg_lo = (t_a - u_start) * kTileTok;
+          e.seg_hi = min((t_b - u_start) * kTileTok, group_len);
+        } else {
+          const long long span = static_cast<long long>(S) * P;
+          const int seg_tokens = static_cast<int>((group_len + span - 1) / span) * P;
+          e.seg_lo = seg * seg_tokens;
+          e.seg_hi = min(e.seg_lo + seg_tokens, group_len);
+        }
+        e.n_tiles = (e.n_rows > 0 && e.seg_lo < e.seg_hi) ? (e.seg_hi - e.seg_lo + kTileTok - 1) / kTileTok : 0;
         if (!good) {
           record_error(p.err, MLA_DEV_BAD_INDPTR);
           e.n_rows = 0;
@@ -650,14 +780,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(4, kNumSoftmaxWarps * 32);
       if (misc.sm_stop[k & 1u]) break;
       const WorkEntry &e = misc.work[ws];
-      const int n_rows = e.n_rows, n_tiles = e.n_tiles, seg = e.seg, e_b = e.b, e_rb = e.rb;
+      const int n_rows = e.n_rows, n_tiles = e.n_tiles, seg = e.seg, e_b = e.b, e_rb = e.rb, fill_hi = e.fill_hi;
       const int row_base = e.row_base, seg_lo = e.seg_lo, seg_hi = e.seg_hi;
       if (n_rows > 0 && n_tiles == 0) {
         // nothing visible in this segment for any row of the block
         if (wq == 0 && my_col < n_rows) {
           const int64_t r = row_base + my_col;
-          if (direct) p.lse[r] = -INFINITY;
-          else { p.segm_max[r * S + seg] = -INFINITY; p.segm_sum[r * S + seg] = 0.0f; }
+          if (direct) {
+            p.lse[r] = -INFINITY;
+          } else {
+            for (int s2 = seg; s2 < max(fill_hi, seg + 1); ++s2) {
+              p.segm_max[r * S + s2] = -INFINITY;
+              p.segm_sum[r * S + s2] = 0.0f;
+            }
+          }
         }
         if (direct && my_col < n_rows) {
           uint4 *dst = reinterpret_cast<uint4 *>(p.out + (row_base + my_col) * 512);
@@ -839,6 +975,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           p.segm_max[r * S + seg] = (l_tot > 0.0f) ? m_ref : -INFINITY;
           p.segm_sum[r * S + seg] = l_tot;
+          for (int s2 = seg + 1; s2 < fill_hi; ++s2) {  // slots of this unit that no part reaches
+            p.segm_max[r * S + s2] = -INFINITY;
+            p.segm_sum[r * S + s2] = 0.0f;
+          }
         }
       }
       const float col_scale = (l_tot > 0.0f) ? (direct ? p.out_scale / l_tot : p.out_scale) : 0.0f;
@@ -986,6 +1126,9 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
   p.num_rows = a.num_rows;
   p.max_len = a.subpage_stride * a.page_size;
   p.tile3d = tile3d ? 1 : 0;
+  const int64_t units = static_cast<int64_t>(a.num_reqs) * V * p.row_blocks;
+  p.num_units = static_cast<int>(units);
+  p.balanced = (a.num_segments >= 2 && (a.flags & MLA_DECODE_UNIFORM_SEGMENTS) == 0 && units <= kMaxUnits) ? 1 : 0;
   const float kv_scale = fp8 ? a.kv_scale : 1.0f;
   p.score_scale_log2 = static_cast<float>(static_cast<double>(a.sm_scale) * kv_scale * 1.4426950408889634);
   p.out_scale = kv_scale;

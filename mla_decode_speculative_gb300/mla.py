@@ -33,6 +33,7 @@ MLA_KV_FP8_E4M3 = 1
 MLA_MERGE_SEGMENTS = 0
 MLA_MERGE_STATES = 1
 MLA_DECODE_SKIP_MERGE = 1
+MLA_DECODE_UNIFORM_SEGMENTS = 2
 
 DEVICE_ERRORS = {0: "MLA_DEV_OK", 1: "MLA_DEV_BAD_INDPTR", 2: "MLA_DEV_BAD_QLEN",
                  3: "MLA_DEV_BAD_BLOCK_ID", 4: "MLA_DEV_LEN_BOUND", 5: "MLA_DEV_BAD_SUBPAGE",
@@ -239,9 +240,11 @@ def decode_verify_workspace_bytes(a: DecodeArgs) -> int:
 
 def decode_verify(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_, num_segments,
                   max_qlen, sm_scale, kv_scale=1.0, out=None, lse=None, workspace=None,
-                  stream=None, skip_merge=False, num_views=1):
+                  stream=None, skip_merge=False, num_views=1, uniform_segments=False):
     """mla_decode_verify.  Returns (out [T, H, 512] bf16, lse [T, H] f32, workspace).
     skip_merge: leave the segment partials in the workspace (MLA_DECODE_SKIP_MERGE).
+    uniform_segments: the pages' equal split per request (MLA_DECODE_UNIFORM_SEGMENTS)
+    instead of the balanced split.
     num_views V > 1: row_len [V, T], subpage_table [V, B, stride]; out [V, T, H, 512],
     lse [V, T, H] (V row views of the same queries, one launch)."""
     T, H, _ = q.shape
@@ -253,7 +256,8 @@ def decode_verify(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_, nu
         lse = torch.empty((*lead, H), dtype=torch.float32, device=q.device)
     a = make_decode_args(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_,
                          num_segments, max_qlen, sm_scale, kv_scale, out, lse,
-                         MLA_DECODE_SKIP_MERGE if skip_merge else 0, num_views=V)
+                         (MLA_DECODE_SKIP_MERGE if skip_merge else 0) |
+                         (MLA_DECODE_UNIFORM_SEGMENTS if uniform_segments else 0), num_views=V)
     need = decode_verify_workspace_bytes(a)
     if need and (workspace is None or workspace.numel() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

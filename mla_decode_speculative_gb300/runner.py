@@ -22,7 +22,7 @@ class VerifyStep:
     def __init__(self, *, num_reqs: int, num_rows: int, num_heads: int, max_qlen: int,
                  block_size: int, num_blocks: int, block_table_width: int, max_kv_len: int,
                  num_segments: int = 1, world_size: int = 1, kv_fp8: bool = False,
-                 interleave: int = 1, device="cuda"):
+                 interleave: int = 1, uniform_segments: bool = False, device="cuda"):
         self.B, self.T, self.H = num_reqs, num_rows, num_heads
         self.max_qlen = max_qlen
         self.block_size = block_size
@@ -30,6 +30,7 @@ class VerifyStep:
         self.W = world_size
         self.interleave = interleave
         self.S = num_segments
+        self.uniform = uniform_segments  # the pages' equal split instead of the balanced one
         self.P = mla.page_size(block_size)
         self.sp_stride = max(1, -(-max_kv_len // self.P))
         self.kv_fp8 = kv_fp8
@@ -63,7 +64,8 @@ class VerifyStep:
                           row_req=self.row_req, subpage_table=self.subpage[0], stream=stream)
             mla.decode_verify(q, kv_cache, qo_indptr, self.row_len, self.subpage[0], self.P,
                               self.S, self.max_qlen, sm_scale, kv_scale, out=self.out,
-                              lse=self.lse, workspace=self.workspace, stream=stream)
+                              lse=self.lse, workspace=self.workspace, stream=stream,
+                              uniform_segments=self.uniform)
             return self.out, self.lse
         mla.plan_rows(seq_lens, qo_indptr, self.T, row_len=self.row_len, row_req=self.row_req,
                       stream=stream)
@@ -75,12 +77,14 @@ class VerifyStep:
         # all W shard views in one decode launch, straight into the shard states
         mla.decode_verify(q, kv_cache, qo_indptr, self.row_len_local, self.subpage, self.P, self.S,
                           self.max_qlen, sm_scale, kv_scale, out=self.part_out, lse=self.part_lse,
-                          workspace=self.workspace, stream=stream, num_views=self.W)
+                          workspace=self.workspace, stream=stream, num_views=self.W,
+                          uniform_segments=self.uniform)
         mla.merge_states(self.part_out, self.part_lse, out=self.out, lse=self.lse, stream=stream)
         return self.out, self.lse
 
 
-def step_for_workload(wl, device="cuda", num_segments: Optional[int] = None) -> VerifyStep:
+def step_for_workload(wl, device="cuda", num_segments: Optional[int] = None,
+                      uniform_segments: bool = False) -> VerifyStep:
     """A VerifyStep sized for a ``workloads.Workload``."""
     return VerifyStep(num_reqs=wl.num_reqs, num_rows=wl.num_rows, num_heads=wl.num_heads,
                       max_qlen=int(wl.qlens.max()), block_size=wl.block_size,
@@ -88,7 +92,7 @@ def step_for_workload(wl, device="cuda", num_segments: Optional[int] = None) -> 
                       max_kv_len=wl.max_kv_len,
                       num_segments=wl.num_segments if num_segments is None else num_segments,
                       world_size=wl.world_size, kv_fp8=(wl.kv_dtype == "fp8"),
-                      interleave=wl.interleave, device=device)
+                      interleave=wl.interleave, uniform_segments=uniform_segments, device=device)
 
 
 def device_inputs(wl, device="cuda"):

@@ -67,9 +67,9 @@ def sample_pairs(wl, n, seed=0):
     return np.stack([r, h], axis=1).astype(np.int32)
 
 
-def run_gpu(wl, num_segments=None, device="cuda"):
+def run_gpu(wl, num_segments=None, device="cuda", uniform_segments=False):
     from mla_decode_speculative_gb300 import runner
-    step = runner.step_for_workload(wl, device, num_segments)
+    step = runner.step_for_workload(wl, device, num_segments, uniform_segments)
     q, kv, seq, ind, bt = runner.device_inputs(wl, device)
     out, lse = step(q, kv, seq, ind, bt, wl.sm_scale, wl.kv_scale)
     torch.cuda.synchronize()

@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
 def test_every_declared_symbol_is_exported(L):
     for n in declared_functions():
         assert hasattr(L, n), f"{n} declared in mla_gb300.h but not exported"
-    assert L.mla_abi_version() == 3
+    assert L.mla_abi_version() == 4
 
 
 def test_page_size_matches_rule(L):

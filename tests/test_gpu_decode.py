@@ -16,8 +16,8 @@ from mla_decode_speculative_gb300 import mla, runner, workloads
 pytestmark = pytest.mark.gpu
 
 
-def _full_check(wl, what, num_segments=None):
-    out, lse, _ = run_gpu(wl, num_segments)
+def _full_check(wl, what, num_segments=None, uniform=False):
+    out, lse, _ = run_gpu(wl, num_segments, uniform_segments=uniform)
     assert mla.get_device_error() == 0
     ref_o, ref_l = oracle_reference(wl)
     return assert_close(out, lse, ref_o, ref_l, what)
@@ -40,9 +40,10 @@ def test_decode_qlen1_bf16_full():
 
 
 @pytest.mark.parametrize("S", [1, 3, 16])
-def test_verify_mtp4_small_every_pair(S):
+@pytest.mark.parametrize("uniform", [False, True])
+def test_verify_mtp4_small_every_pair(S, uniform):
     wl = workloads.verify_mtp4_bf16(seed=1, batch=5, lo=130, hi=1500, num_segments=S)
-    _full_check(wl, f"verify qlen=4, S={S}")
+    _full_check(wl, f"verify qlen=4, S={S}, uniform={uniform}", uniform=uniform)
 
 
 def test_fp8_small_every_pair():
@@ -87,9 +88,11 @@ def test_dcp_interleaved_every_pair(W, I):
 
 @pytest.mark.parametrize("S", [1, 3])
 def test_row_views_in_one_launch_equal_separate_calls(S):
-    """num_views = W decodes the W shard row views in one launch; every view's
-    output must equal, bit for bit, its own single-view call (each work item
-    runs the same arithmetic either way)."""
+    """num_views = W decodes the W shard row views in one launch.  With the
+    pages' split every view's output equals, bit for bit, its own single-view
+    call (each work item runs the same arithmetic either way); the balanced
+    split cuts a different set of chunks, so there both agree with the oracle's
+    shard states."""
     W = 4
     wl = workloads.make_workload("views", [700, 90, 1500, 33], [4, 3, 8, 2], 16, 16,
                                  world_size=W, num_segments=S, seed=11)
@@ -97,13 +100,21 @@ def test_row_views_in_one_launch_equal_separate_calls(S):
     q, kv, seq, ind, bt = runner.device_inputs(wl, "cuda")
     step(q, kv, seq, ind, bt, wl.sm_scale)  # fills the row views and sub-page tables
     torch.cuda.synchronize()
-    all_out, all_lse, _ = mla.decode_verify(q, kv, ind, step.row_len_local, step.subpage, step.P, S,
-                                            int(wl.qlens.max()), wl.sm_scale, num_views=W)
+    Q = int(wl.qlens.max())
+    all_out, all_lse, _ = mla.decode_verify(q, kv, ind, step.row_len_local, step.subpage, step.P, S, Q,
+                                            wl.sm_scale, num_views=W, uniform_segments=True)
+    bal_out, bal_lse, _ = mla.decode_verify(q, kv, ind, step.row_len_local, step.subpage, step.P, S, Q,
+                                            wl.sm_scale, num_views=W)
+    row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
+    _, _, ref_po, ref_pl = oracle.sharded_attention(wl.qo_indptr, row_len, wl.q_bits(), wl.kv_host(),
+                                                    wl.kv_scale, wl.sm_scale, wl.block_tables,
+                                                    wl.block_size, W)
     for r in range(W):
-        o, l, _ = mla.decode_verify(q, kv, ind, step.row_len_local[r], step.subpage[r], step.P, S,
-                                    int(wl.qlens.max()), wl.sm_scale)
+        o, l, _ = mla.decode_verify(q, kv, ind, step.row_len_local[r], step.subpage[r], step.P, S, Q,
+                                    wl.sm_scale, uniform_segments=True)
         torch.cuda.synchronize()
         assert torch.equal(o, all_out[r]) and torch.equal(l, all_lse[r]), f"view {r}"
+        assert_close(bal_out[r], bal_lse[r], ref_po[r], ref_pl[r], f"balanced, view {r}")
     assert mla.get_device_error() == 0
 
 
@@ -143,7 +154,7 @@ def test_nan_in_unused_cache_slots_is_never_read():
 
 def test_segment_partials_match_oracle():
     wl = workloads.verify_mtp4_bf16(seed=7, batch=3, lo=300, hi=1300, num_segments=5)
-    out, lse, step = run_gpu(wl)
+    out, lse, step = run_gpu(wl, uniform_segments=True)  # the pages' split, slot by slot
     segm_out, segm_max, segm_sum = mla.workspace_views(step.workspace, wl.num_reqs, int(wl.qlens.max()),
                                                        wl.num_rows, wl.num_heads, 5)
     row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
@@ -162,6 +173,91 @@ def test_segment_partials_match_oracle():
     lse2_ref = mx[live] + np.log2(sm[live])
     lse2_gpu = gm[live] + np.log2(gs[live])
     assert np.abs(lse2_gpu - lse2_ref).max() * math.log(2) <= 1e-3
+
+
+def _balanced_parts(unit_tiles, S, grid):
+    """The balanced split as the header states it, restated for the test: the
+    units' T tiles end to end, n chunks [floor(cT/n), floor((c+1)T/n)) with
+    n = min(grid, T // need), need = ceil(tmax / (S-1)) (so no unit meets more
+    than S chunks); unit u's part in chunk c is its segment c - (chunk of its
+    first tile).  Returns {u: [(tile_lo, tile_hi) per segment]}."""
+    T, tmax = sum(unit_tiles), max(unit_tiles)
+    need = max(-(-tmax // (S - 1)), 1)
+    n = min(grid, max(T // need, 1)) if T else 1
+    bounds = [c * T // n for c in range(n + 1)]
+    parts, start = {}, 0
+    for u, t in enumerate(unit_tiles):
+        parts[u] = [(max(bounds[c], start) - start, min(bounds[c + 1], start + t) - start)
+                    for c in range(n) if t and bounds[c] < start + t and bounds[c + 1] > start]
+        start += t
+    return parts
+
+
+@pytest.mark.parametrize("S", [2, 5, 16])
+def test_balanced_split_slots_and_merge(S):
+    """Balanced split (the default): which (row, slot) pairs hold a part is
+    fixed by the rule above, slots past a unit's parts are empty (max = -inf,
+    sum = 0), and merging the kernel's own bf16 partials in float64 gives the
+    oracle's attention -- every visible token counted once."""
+    wl = workloads.verify_mtp4_bf16(seed=11, batch=9, lo=40, hi=5000, num_segments=S)
+    out, lse, step = run_gpu(wl)
+    assert mla.get_device_error() == 0
+    H, B = wl.num_heads, wl.num_reqs
+    RB = mla.row_blocks(int(wl.qlens.max()), H)
+    segm_out, segm_max, segm_sum = mla.workspace_views(step.workspace, B, int(wl.qlens.max()),
+                                                       wl.num_rows, H, S)
+    gm, gs = segm_max.cpu().numpy(), segm_sum.cpu().numpy()
+    row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
+    ind = wl.qo_indptr
+    units = []
+    for b in range(B):
+        ln = int(max(row_len[ind[b]:ind[b + 1]]))
+        rows = (ind[b + 1] - ind[b]) * H
+        units += [(-(-ln // 64)) if rb * 64 < rows else 0 for rb in range(RB)]
+    grid = min(torch.cuda.get_device_properties(0).multi_processor_count, B * RB * S)
+    parts = _balanced_parts(units, S, grid)
+    assert max(len(v) for v in parts.values()) <= S
+    for b in range(B):
+        for t in range(ind[b], ind[b + 1]):
+            for h in range(H):
+                rr = (t - ind[b]) * H + h
+                pl = parts[b * RB + rr // 64]
+                for s in range(S):
+                    live = s < len(pl) and pl[s][0] * 64 < row_len[t]
+                    assert np.isneginf(gm[t, h, s]) == (not live), (b, t, h, s)
+                    if not live:
+                        assert gs[t, h, s] == 0.0
+    go = blocks_to_rows(segm_out.float().cpu().numpy(), ind, H, wl.num_rows)
+    live = ~np.isneginf(gm)
+    acc = np.where(live[..., None], go, 0.0).astype(np.float64)
+    mo, ml = oracle.merge_segments(acc, np.where(live, gm, -np.inf).astype(np.float64),
+                                   np.where(live, gs, 0.0).astype(np.float64))
+    ref_o, ref_l = oracle_reference(wl)
+    assert_close(torch.tensor(mo), torch.tensor(ml), ref_o, ref_l, f"merged kernel partials, S={S}")
+
+
+@pytest.mark.parametrize("uniform", [False, True])
+def test_poisoned_workspace_is_never_read(uniform):
+    """Every segment slot the merge reads is written by the call: a workspace
+    full of NaN bit patterns beforehand changes nothing."""
+    wl = workloads.dcp8_verify_bf16(seed=12, batch=3, context=2500, world_size=4, num_segments=6)
+    step = runner.step_for_workload(wl, "cuda", uniform_segments=uniform)
+    q, kv, seq, ind, bt = runner.device_inputs(wl, "cuda")
+    step.workspace.fill_(0xFF)
+    out, lse = step(q, kv, seq, ind, bt, wl.sm_scale, wl.kv_scale)
+    torch.cuda.synchronize()
+    assert mla.get_device_error() == 0
+    ref_o, ref_l = oracle_reference(wl)
+    assert_close(out, lse, ref_o, ref_l, f"poisoned workspace, uniform={uniform}")
+
+
+def test_more_units_than_the_balanced_table_uses_the_uniform_split():
+    """1030 requests of one row each (more (view, request, row block) units
+    than the balanced split tabulates): the call takes the pages' split."""
+    rng = np.random.default_rng(13)
+    L = rng.integers(1, 200, 1030)
+    wl = workloads.make_workload("many_units", L, np.ones(1030, np.int64), 4, 16, num_segments=3, seed=13)
+    _full_check(wl, "1030 single-row requests, S=3")
 
 
 def test_static_bound_does_not_change_results():
