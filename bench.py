@@ -74,32 +74,79 @@ def kv_bytes(wl) -> int:
     return int(wl.seq_lens.astype(np.int64).sum()) * per_tok
 
 
-def decode_unit_bytes(wl) -> dict:
+def _balanced_parts(unit_tiles, S, grid):
+    """Tile ranges of the balanced split's parts, per unit (the rule of
+    MLA_DECODE_UNIFORM_SEGMENTS's default in the C header): the units' T tiles
+    end to end, n = min(grid, T // ceil(tmax / (S-1))) chunks
+    [floor(cT/n), floor((c+1)T/n)); a unit's part in chunk c is one segment."""
+    T, tmax = int(sum(unit_tiles)), int(max(unit_tiles))
+    need = max(-(-tmax // (S - 1)), 1)
+    n = min(grid, max(T // need, 1)) if T else 1
+    bounds = [c * T // n for c in range(n + 1)]
+    parts, start = [], 0
+    for t in unit_tiles:
+        t = int(t)
+        c0 = next((c for c in range(n) if bounds[c + 1] > start), n) if t else n
+        lst = []
+        c = c0
+        while t and c < n and bounds[c] < start + t:
+            lst.append((max(bounds[c], start) - start, min(bounds[c + 1], start + t) - start))
+            c += 1
+        parts.append(lst)
+        start += t
+    return parts
+
+
+def decode_unit_bytes(wl, grid=None) -> dict:
     """Algorithmic bytes of one launch of the decode kernel (all shard views
     of a sharded step in the one launch): visible KV rows, the query rows
     (once per view), and the split-K partials it must write (an (m, l) pair
-    for every (view, row, head, segment), a 1 KiB bf16 vector for every one
-    that holds a visible token)."""
+    for every (view, row, head, segment slot), a 1 KiB bf16 vector for every
+    (row, head, part) that holds a visible token).  Parts follow the split
+    the call takes: balanced (S > 1, at most 1024 (view, request, row block)
+    units; grid = the launch's CTAs) or the pages' equal split."""
     P = min(128, wl.block_size & -wl.block_size)
     S = wl.num_segments
-    W, I = wl.world_size, wl.interleave
+    W, I, H, B = wl.world_size, wl.interleave, wl.num_heads, wl.num_reqs
 
     def local(w, r):  # positions of a window of w that shard r holds (runs of I dealt in turn)
         rem = min(max(w % (I * W) - r * I, 0), I)
         return (w // (I * W)) * I + rem
 
+    RB = -(-int(max(wl.qlens)) * H // 64)
+    balanced = S > 1 and W * B * RB <= 1024
     active = 0
-    for r in range(W):
-        for b in range(wl.num_reqs):
-            L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
-            tps_tok = max(1, -(-local(L, r) // (S * P))) * P
-            for t in range(ql):
-                active += -(-local(L - ql + 1 + t, r) // tps_tok)
-    heads = wl.num_heads
+    if balanced:
+        if grid is None:
+            import torch
+            grid = torch.cuda.get_device_properties(0).multi_processor_count
+        grid = min(grid, W * B * RB * S)
+        units = []
+        for r in range(W):
+            for b in range(B):
+                L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
+                ln = max(local(L - ql + 1 + t, r) for t in range(ql))
+                units += [-(-ln // 64) if rb * 64 < ql * H else 0 for rb in range(RB)]
+        parts = _balanced_parts(units, S, grid)
+        for r in range(W):
+            for b in range(B):
+                L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
+                for t in range(ql):
+                    w = local(L - ql + 1 + t, r)
+                    for h in range(H):
+                        pl = parts[(r * B + b) * RB + (t * H + h) // 64]
+                        active += sum(1 for lo, _ in pl if lo * 64 < w)
+    else:
+        for r in range(W):
+            for b in range(B):
+                L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
+                tps_tok = max(1, -(-local(L, r) // (S * P))) * P
+                for t in range(ql):
+                    active += -(-local(L - ql + 1 + t, r) // tps_tok) * H
     kv = kv_bytes(wl)
-    q = W * wl.num_rows * heads * 1152  # each shard view reads the queries
-    partial = (W * wl.num_rows * heads * S * 8 + active * heads * 1024) if S > 1 else \
-        W * wl.num_rows * heads * (1024 + 4)
+    q = W * wl.num_rows * H * 1152  # each shard view reads the queries
+    partial = (W * wl.num_rows * H * S * 8 + active * 1024) if S > 1 else \
+        W * wl.num_rows * H * (1024 + 4)
     return {"kv": kv, "q": q, "partials": partial, "total": kv + q + partial}
 
 

@@ -11,17 +11,20 @@
 // natural-log LSE directly.
 //
 // GB300 design (not the pages' ROCm design):
-//  * Work item = (request, row view, block of <= 64 query rows, split-K
-//    segment).  The rows of a request (heads x qlen) are decoded jointly
-//    against shared 64-token KV tiles, so each latent row is read from HBM
-//    once per request (the pages replicate the request once per verify row);
-//    several row views of the same queries (the shard views of a DCP step)
-//    can share one launch.
-//  * Persistent CTAs, one per SM.  The producer warp claims items from an
-//    atomic counter (dynamic load balance, longest requests first) and
-//    publishes each decoded item, with its rows' visible lengths, through a
-//    4-deep shared-memory work ring.  Every barrier phase follows one running
-//    tile counter.
+//  * Work entry = (row view, request, block of <= 64 query rows, split-K
+//    segment slot, token range).  The rows of a request (heads x qlen) are
+//    decoded jointly against shared 64-token KV tiles, so each latent row is
+//    read from HBM once per request (the pages replicate the request once per
+//    verify row); several row views of the same queries (the shard views of a
+//    DCP step) can share one launch.
+//  * Persistent CTAs, one per SM.  Balanced split (default): every CTA
+//    tabulates the tiles of all (view, request, row block) units, and the
+//    producer warp claims equal chunks of the units' concatenated tiles from
+//    an atomic counter; a chunk's part of each unit it meets is one segment
+//    of that unit.  With the pages' equal split the producer claims (unit,
+//    segment) items, longest requests first.  Entries, with their rows'
+//    visible lengths, go to the other roles through a 4-deep shared-memory
+//    work ring.  Every barrier phase follows one running tile counter.
 //  * Swapped operand order, so the output accumulator fits TMEM densely:
 //        S^T[64 tok, 64 rows]     = K_tile[64, 576] . Q[64, 576]^T      (M = 64, K-major A and B)
 //        O^T[4x128 dims, 64 rows] += V^T[512, 64 tok] . P^T[64, 64]^T   (M = 128, MN-major A and B)
