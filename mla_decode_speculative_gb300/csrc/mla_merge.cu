@@ -18,7 +18,7 @@
 // CTA merges 64 output dims of one row block: warp w takes dims 8w..8w+7 of
 // the CTA's 64, lane l the rows of octet l/4 for two of those dims, so every
 // segment costs a warp two 16-byte loads per lane over eight 128-byte runs
-// (four segments in flight), with per-row weights staged in shared memory;
+// (the live segments eight at a time), with per-row weights staged in shared memory;
 // the merged 64 x 64 tile is transposed in shared memory and written as
 // 128-byte row pieces.
 // State partials are row-major [W][T*H][512] bf16: one 128-thread block per
@@ -84,14 +84,17 @@ __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x 
 constexpr int kSegChunk = 32;  // segments whose weights are staged at a time
 
 // grid (B * RB, 512 / 64), 256 threads.  The block's 64 rows x S statistics
-// are contiguous; the CTA stages per-row maxima, then normalised weights
-// 2^(m_s - M) / den for 32 segments at a time, in shared memory, and streams
-// the partial blocks four segments deep.
+// are contiguous; one pass gives every row its max and denominator (a
+// running pair per thread, rescaled as the max grows), then the normalised
+// weights 2^(m_s - M) / den of 32 segments at a time go to shared memory, the
+// segments with a non-zero weight are listed, and their partial blocks are
+// read eight at a time.
 __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
   __shared__ __align__(16) float s_w[kSegChunk][kBlockRows];
   __shared__ __align__(16) uint32_t s_o[kBlockRows][kDimsPerCta / 2 + 4];  // bf16 pairs, padded rows
   __shared__ int s_live[kSegChunk];
-  __shared__ float s_part[4][kBlockRows];
+  __shared__ float s_part[4][kBlockRows], s_dpart[4][kBlockRows];
+  __shared__ int s_list[kSegChunk], s_nlive;
   __shared__ float s_M[kBlockRows], s_inv[kBlockRows];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // block (view, request, row block): vb = v * B + b
@@ -107,25 +110,34 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
   const float *mx = p.segm_max + grow0 * S;  // [64 rows][S], contiguous
   const float *sm = p.segm_sum + grow0 * S;
 
-  // per-row max and denominator: four threads per row, segments strided by 4
+  // per-row max and denominator in one pass: four threads per row, segments
+  // strided by 4, each keeping a running (max, sum) rescaled as the max grows
   const int row = tid & (kBlockRows - 1), quarter = tid >> 6;
-  float M = -INFINITY;
+  float Mq = -INFINITY, dq = 0.0f;
   if (row < n_rows)
-    for (int s = quarter; s < S; s += 4) M = fmaxf(M, mx[row * S + s]);
-  s_part[quarter][row] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(s_part[0][row], s_part[1][row]), fmaxf(s_part[2][row], s_part[3][row]));
-  __syncthreads();
-  float d = 0.0f;
-  if (row < n_rows && M != -INFINITY)
     for (int s = quarter; s < S; s += 4) {
       const float m = mx[row * S + s];
-      if (m != -INFINITY) d += exp2f(m - M) * sm[row * S + s];
+      if (m == -INFINITY) continue;
+      const float l = sm[row * S + s];
+      if (m > Mq) {
+        dq = dq * exp2f(Mq - m) + l;  // 0 while Mq is -inf
+        Mq = m;
+      } else {
+        dq += exp2f(m - Mq) * l;
+      }
     }
-  s_part[quarter][row] = d;
+  s_part[quarter][row] = Mq;
+  s_dpart[quarter][row] = dq;
   __syncthreads();
   if (quarter == 0) {
-    d = s_part[0][row] + s_part[1][row] + s_part[2][row] + s_part[3][row];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) M = fmaxf(M, s_part[k][row]);
+    float d = 0.0f;
+    if (M != -INFINITY)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (s_part[k][row] != -INFINITY) d += exp2f(s_part[k][row] - M) * s_dpart[k][row];
     s_M[row] = M;
     s_inv[row] = d > 0.0f ? 1.0f / d : 0.0f;
     if (blockIdx.y == 0 && row < n_rows)
@@ -156,13 +168,20 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
       if (w != 0.0f) s_live[sc] = 1;
     }
     __syncthreads();
-    for (int sc0 = 0; sc0 < nc; sc0 += 4) {
-      uint4 x[4][2];
+    if (warp == 0) {  // the chunk's live slots, in order
+      const bool lv = lane < nc && s_live[lane] != 0;
+      const unsigned mk = __ballot_sync(0xffffffffu, lv);
+      if (lv) s_list[__popc(mk & ((1u << lane) - 1u))] = lane;
+      if (lane == 0) s_nlive = __popc(mk);
+    }
+    __syncthreads();
+    const int n_live = s_nlive;
+    for (int i0 = 0; i0 < n_live; i0 += 8) {
+      uint4 x[8][2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int sc = sc0 + u;
-        if (sc < nc && s_live[sc]) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + c0 + sc) * (512 * kBlockRows)) +
+      for (int u = 0; u < 8; ++u) {
+        if (i0 + u < n_live) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + c0 + s_list[i0 + u]) * (512 * kBlockRows)) +
                              oct * 512 + dim0 + dp;
           x[u][0] = __ldcs(src);
           x[u][1] = __ldcs(src + 1);
@@ -172,9 +191,9 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
       }
       // a weight of 0 selects 0: an empty row's slot is never used as a value
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int sc = sc0 + u;
-        if (sc >= nc || !s_live[sc]) continue;
+      for (int u = 0; u < 8; ++u) {
+        if (i0 + u >= n_live) break;
+        const int sc = s_list[i0 + u];
         const float4 wa = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oct]);
         const float4 wb = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oct + 4]);
         const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
