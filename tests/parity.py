@@ -101,3 +101,21 @@ def blocks_to_rows(blocks, qo_indptr, num_heads, num_rows):
         for i in range(r1 - r0):
             out[r0 + i] = blocks[b, i // 64, :, (i % 64) // 8, :, i % 8]
     return out.reshape(num_rows, num_heads, S, D)
+
+
+def balanced_parts(unit_tiles, S, grid):
+    """The balanced split as the header states it, restated for the test: the
+    units' T tiles end to end, n chunks [floor(cT/n), floor((c+1)T/n)) with
+    n = min(grid, T // need), need = ceil(tmax / (S-1)) (so no unit meets more
+    than S chunks); unit u's part in chunk c is its segment c - (chunk of its
+    first tile).  Returns {u: [(tile_lo, tile_hi) per segment]}."""
+    T, tmax = sum(unit_tiles), max(unit_tiles)
+    need = max(-(-tmax // (S - 1)), 1)
+    n = min(grid, max(T // need, 1)) if T else 1
+    bounds = [c * T // n for c in range(n + 1)]
+    parts, start = {}, 0
+    for u, t in enumerate(unit_tiles):
+        parts[u] = [(max(bounds[c], start) - start, min(bounds[c + 1], start + t) - start)
+                    for c in range(n) if t and bounds[c] < start + t and bounds[c + 1] > start]
+        start += t
+    return parts

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from parity import assert_close, blocks_to_rows, oracle_reference, run_gpu, sample_pairs
+from parity import assert_close, balanced_parts, blocks_to_rows, oracle_reference, run_gpu, sample_pairs
 from mla_decode_speculative_gb300 import mla, runner, workloads
 
 pytestmark = pytest.mark.gpu
@@ -175,24 +175,6 @@ def test_segment_partials_match_oracle():
     assert np.abs(lse2_gpu - lse2_ref).max() * math.log(2) <= 1e-3
 
 
-def _balanced_parts(unit_tiles, S, grid):
-    """The balanced split as the header states it, restated for the test: the
-    units' T tiles end to end, n chunks [floor(cT/n), floor((c+1)T/n)) with
-    n = min(grid, T // need), need = ceil(tmax / (S-1)) (so no unit meets more
-    than S chunks); unit u's part in chunk c is its segment c - (chunk of its
-    first tile).  Returns {u: [(tile_lo, tile_hi) per segment]}."""
-    T, tmax = sum(unit_tiles), max(unit_tiles)
-    need = max(-(-tmax // (S - 1)), 1)
-    n = min(grid, max(T // need, 1)) if T else 1
-    bounds = [c * T // n for c in range(n + 1)]
-    parts, start = {}, 0
-    for u, t in enumerate(unit_tiles):
-        parts[u] = [(max(bounds[c], start) - start, min(bounds[c + 1], start + t) - start)
-                    for c in range(n) if t and bounds[c] < start + t and bounds[c + 1] > start]
-        start += t
-    return parts
-
-
 @pytest.mark.parametrize("S", [2, 5, 16])
 def test_balanced_split_slots_and_merge(S):
     """Balanced split (the default): which (row, slot) pairs hold a part is
@@ -215,7 +197,7 @@ def test_balanced_split_slots_and_merge(S):
         rows = (ind[b + 1] - ind[b]) * H
         units += [(-(-ln // 64)) if rb * 64 < rows else 0 for rb in range(RB)]
     grid = min(torch.cuda.get_device_properties(0).multi_processor_count, B * RB * S)
-    parts = _balanced_parts(units, S, grid)
+    parts = balanced_parts(units, S, grid)
     assert max(len(v) for v in parts.values()) <= S
     for b in range(B):
         for t in range(ind[b], ind[b + 1]):
