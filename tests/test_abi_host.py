@@ -73,6 +73,14 @@ def test_host_validation_without_cuda(L):
     a.num_segments = 4
     assert L.mla_decode_verify_workspace(ctypes.byref(a)) > 0
     assert L.mla_decode_verify(ctypes.byref(a), None, 0, None) == mla.MLA_ERR_WORKSPACE
+    # the split flag is a known flag (the call then stops at the missing workspace);
+    # an unknown flag bit is rejected before anything else happens
+    a.flags = mla.MLA_DECODE_UNIFORM_SEGMENTS | mla.MLA_DECODE_SKIP_MERGE
+    assert L.mla_decode_verify(ctypes.byref(a), None, 0, None) == mla.MLA_ERR_WORKSPACE
+    a.flags = 4
+    assert L.mla_decode_verify(ctypes.byref(a), None, 0, None) == mla.MLA_ERR_INVALID_ARG
+    assert b"flags" in L.mla_last_error_string()
+    a.flags = 0
     a.q = 258  # misaligned
     assert L.mla_decode_verify(ctypes.byref(a), None, 0, None) == mla.MLA_ERR_INVALID_ARG
     # merge: unknown mode
