@@ -114,7 +114,8 @@ def decode_unit_bytes(wl, grid=None) -> dict:
         return (w // (I * W)) * I + rem
 
     RB = -(-int(max(wl.qlens)) * H // 64)
-    balanced = S > 1 and W * B * RB <= 1024
+    max_len = max(1, -(-int(wl.max_kv_len) // P)) * P  # the static bound the step passes
+    balanced = S > 1 and W * B * RB <= 1024 and W * B * RB * -(-max_len // 64) <= 2 ** 31 - 1
     active = 0
     if balanced:
         if grid is None:

@@ -1131,7 +1131,12 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
   p.tile3d = tile3d ? 1 : 0;
   const int64_t units = static_cast<int64_t>(a.num_reqs) * V * p.row_blocks;
   p.num_units = static_cast<int>(units);
-  p.balanced = (a.num_segments >= 2 && (a.flags & MLA_DECODE_UNIFORM_SEGMENTS) == 0 && units <= kMaxUnits) ? 1 : 0;
+  // the balanced split counts tiles in int32: every unit at the static bound must fit
+  const int64_t max_unit_tiles = (static_cast<int64_t>(a.subpage_stride) * a.page_size + kTileTok - 1) / kTileTok;
+  p.balanced = (a.num_segments >= 2 && (a.flags & MLA_DECODE_UNIFORM_SEGMENTS) == 0 && units <= kMaxUnits &&
+                units * max_unit_tiles <= INT32_MAX)
+                   ? 1
+                   : 0;
   const float kv_scale = fp8 ? a.kv_scale : 1.0f;
   p.score_scale_log2 = static_cast<float>(static_cast<double>(a.sm_scale) * kv_scale * 1.4426950408889634);
   p.out_scale = kv_scale;
