@@ -85,6 +85,10 @@ def _load():
                                                     c_dbl, c_dbl, i32p, c_int, c_int, c_int, c_int,
                                                     f64p, f64p, f64p]
             lib.oracle_segment_partials.restype = c_int
+            lib.oracle_range_partials.argtypes = [c_int, c_int, c_int, i32p, i32p, vp, vp, c_int, c_i64,
+                                                  c_dbl, c_dbl, i32p, c_int, c_int, c_int,
+                                                  ctypes.POINTER(ctypes.c_int64), f64p, f64p, f64p]
+            lib.oracle_range_partials.restype = c_int
             lib.oracle_merge_segments.argtypes = [c_i64, c_int, f64p, f64p, f64p, f64p, f64p]
             lib.oracle_merge_segments.restype = None
             lib.oracle_merge_states.argtypes = [c_i64, c_int, f64p, f64p, f64p, f64p]
@@ -274,6 +278,38 @@ def segment_partials(qo_indptr, row_len, q_bits, kv, kv_scale, sm_scale, block_t
                                            bt.shape[1], int(block_size), S, int(tile_size),
                                            ap, mp, smp)
     _check(code, "segment_partials")
+    return acc, mx, sm
+
+
+def range_partials(qo_indptr, row_len, q_bits, kv, kv_scale, sm_scale, block_table,
+                   block_size, ranges):
+    """Base-2 partials per (row, head, slot) over given token ranges
+    [vLLM #51705, 实现拆解 4: a segment's local max, exp2 sum and output]:
+    ranges [B, G, S, 2] int64 = [lo, hi) of slot s for the 64-row group g of
+    request b (row (t, h) of b is in group ((t - q0) * H + h) // 64).
+    Returns (acc [T,H,S,512], m [T,H,S], l [T,H,S])."""
+    ind, ip = _i32(qo_indptr)
+    rl, rp = _i32(row_len)
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    T, H, _ = q.shape
+    kv, dt = _kv_args(kv)
+    bt, bp = _i32(block_table)
+    rg = np.ascontiguousarray(ranges, dtype=np.int64)
+    B, G, S, two = rg.shape
+    if B != ind.shape[0] - 1 or two != 2:
+        raise ValueError("ranges must be [B, G, S, 2]")
+    acc = np.zeros((T, H, S, D_V), np.float64)
+    mx = np.zeros((T, H, S), np.float64)
+    sm = np.zeros((T, H, S), np.float64)
+    _, ap = _f64(acc)
+    _, mp = _f64(mx)
+    _, smp = _f64(sm)
+    code = _load().oracle_range_partials(B, H, G, ip, rp, q.ctypes.data, kv.ctypes.data, dt,
+                                         kv.shape[0], float(kv_scale), float(sm_scale), bp,
+                                         bt.shape[1], int(block_size), S,
+                                         rg.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                         ap, mp, smp)
+    _check(code, "range_partials")
     return acc, mx, sm
 
 

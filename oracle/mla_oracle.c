@@ -404,6 +404,92 @@ int oracle_segment_partials(int num_reqs, int num_heads,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Partials over caller-chosen token ranges.  The segmented decode keeps, per
+ * segment, the local base-2 max, the exp2 sum and the unnormalised output of
+ * the tokens in the segment's range [vLLM #51705, 实现拆解 4]; the pages cut
+ * those ranges by the rule of oracle_segment_partials.  This function takes
+ * the ranges as given, so that any partition of a request's tokens can be
+ * checked slot by slot: row (t, h) of request b belongs to 64-row group
+ * g = ((t - qo_indptr[b]) * H + h) / 64, and its slot s covers the tokens
+ * [lo, hi) = ranges[((b * groups + g) * S + s) * 2 + {0, 1}] that the row
+ * can see (j < row_len).  Per (row, head, slot), as oracle_segment_partials:
+ *   m_s = max_j x_j, l_s = sum_j 2^(x_j - m_s), acc_s = sum_j 2^(x_j - m_s) vhat[j,:]
+ * (-inf, 0, 0 for no visible token).  Output layout as there.               */
+int oracle_range_partials(int num_reqs, int num_heads, int groups,
+                          const int32_t *qo_indptr, const int32_t *row_len,
+                          const uint16_t *q, const void *kv, int kv_dtype,
+                          int64_t kv_rows, double kv_scale, double sm_scale,
+                          const int32_t *block_table, int bt_stride,
+                          int block_size, int num_slots, const int64_t *ranges,
+                          double *acc, double *mx, double *sm) {
+  const double LOG2E = 1.0 / log(2.0);
+  int num_rows = qo_indptr[num_reqs];
+  int S = num_slots;
+  int err = ORC_OK;
+  (void)kv_rows;
+  if (S < 1 || groups < 1) return ORC_ERR_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t it = 0; it < (int64_t)num_rows * num_heads; it++) {
+    int row = (int)(it / num_heads);
+    int h = (int)(it % num_heads);
+    int b = request_of_row(num_reqs, qo_indptr, row);
+    if (b < 0) {
+#pragma omp atomic write
+      err = ORC_ERR_ARG;
+      continue;
+    }
+    int g = ((row - qo_indptr[b]) * num_heads + h) / 64;
+    if (g >= groups) {
+#pragma omp atomic write
+      err = ORC_ERR_ARG;
+      continue;
+    }
+    const uint16_t *qv = q + ((int64_t)row * num_heads + h) * ORC_DK;
+    double qd[ORC_DK];
+    for (int d = 0; d < ORC_DK; d++) qd[d] = bf16_bits_to_double(qv[d]);
+    for (int s = 0; s < S; s++) {
+      int64_t base = it * S + s;
+      double *a = acc + base * ORC_DV;
+      for (int d = 0; d < ORC_DV; d++) a[d] = 0.0;
+      mx[base] = -INFINITY;
+      sm[base] = 0.0;
+      const int64_t *rg = ranges + (((int64_t)b * groups + g) * S + s) * 2;
+      int64_t lo = rg[0] < 0 ? 0 : rg[0];
+      int64_t hi = rg[1];
+      if (hi > row_len[row]) hi = row_len[row];
+      if (lo >= hi) continue;
+      double *x = (double *)malloc(sizeof(double) * (size_t)(hi - lo));
+      if (!x) {
+#pragma omp atomic write
+        err = ORC_ERR_NOMEM;
+        break;
+      }
+      double m = -INFINITY;
+      for (int64_t j = lo; j < hi; j++) {
+        int64_t slot = slot_of_token(block_table, bt_stride, b, j, block_size);
+        double dot = 0.0;
+        for (int d = 0; d < ORC_DK; d++)
+          dot += qd[d] * cached_value(kv, kv_dtype, slot, d, kv_scale);
+        x[j - lo] = sm_scale * dot * LOG2E;
+        if (x[j - lo] > m) m = x[j - lo];
+      }
+      double l = 0.0;
+      for (int64_t j = lo; j < hi; j++) {
+        int64_t slot = slot_of_token(block_table, bt_stride, b, j, block_size);
+        double e = exp2(x[j - lo] - m);
+        l += e;
+        for (int d = 0; d < ORC_DV; d++)
+          a[d] += e * cached_value(kv, kv_dtype, slot, d, kv_scale);
+      }
+      mx[base] = m;
+      sm[base] = l;
+      free(x);
+    }
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Segment merge.  [vLLM #51705, 实现拆解 4 and the merge_mla_segments_triton
  * snippet]: base-2 segment statistics are combined into one output and a
  * natural-log LSE (the LOGE2 constant there is ln 2):

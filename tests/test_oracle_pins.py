@@ -364,6 +364,66 @@ def test_segment_partials_merge_to_attention(S):
     assert np.isneginf(mx[0, 0, active:]).all() and np.isfinite(mx[3, 0, :active]).all()
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_range_partials_over_any_partition_merge_to_attention(seed):
+    """Partials over arbitrary contiguous cuts of each 64-row group's tokens
+    (some slots empty, some past the rows' windows) merge to the attention."""
+    rng = np.random.default_rng(40 + seed)
+    seq, ql, H, bs = [300, 70, 129, 5], [4, 1, 3, 2], 40, 16  # 40 heads: groups of 64 rows split tokens
+    dense, pool, bt, q, ind = _rand_case(rng, seq, ql, H, bs)
+    row_len, _, _ = oracle.plan_rows(seq, ind)
+    B, S = len(seq), 6
+    G = -(-max(ql) * H // 64)
+    ranges = np.zeros((B, G, S, 2), np.int64)
+    for b in range(B):
+        for g in range(G):
+            cuts = np.sort(rng.integers(0, seq[b] + 1, S - 1))
+            edges = np.concatenate([[0], cuts, [seq[b] + int(rng.integers(0, 40))]])
+            ranges[b, g, :, 0], ranges[b, g, :, 1] = edges[:-1], edges[1:]
+    acc, mx, sm = oracle.range_partials(ind, row_len, q, pool, 1.0, SM, bt, bs, ranges)
+    out, lse = oracle.merge_segments(acc, mx, sm)
+    ref_out, ref_lse = oracle.attention(ind, row_len, q, pool, 1.0, SM, bt, bs)
+    np.testing.assert_allclose(out, ref_out, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+    # a slot is empty exactly when its range holds none of the row's visible tokens
+    for t in range(int(ind[-1])):
+        b = int(np.searchsorted(ind, t, side="right") - 1)
+        for h in range(H):
+            g = ((t - ind[b]) * H + h) // 64
+            for s_ in range(S):
+                lo, hi = ranges[b, g, s_]
+                assert np.isneginf(mx[t, h, s_]) == (min(hi, row_len[t]) <= lo)
+
+
+def test_range_partials_single_token_and_pages_split():
+    """A one-token range holds that token's V row with l = 1; the pages'
+    ranges reproduce oracle_segment_partials exactly."""
+    rng = np.random.default_rng(44)
+    seq, ql, H, bs = [90, 33], [3, 1], 2, 16
+    dense, pool, bt, q, ind = _rand_case(rng, seq, ql, H, bs)
+    row_len, _, _ = oracle.plan_rows(seq, ind)
+    ranges = np.zeros((2, 1, 2, 2), np.int64)
+    ranges[:, 0, 0] = [7, 8]          # token 7 alone
+    ranges[:, 0, 1] = [200, 300]      # past every window: empty
+    acc, mx, sm = oracle.range_partials(ind, row_len, q, pool, 1.0, SM, bt, bs, ranges)
+    for t in range(4):
+        b = 0 if t < 3 else 1
+        v7 = (dense[b][7, :D_V].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        for h in range(H):
+            assert sm[t, h, 0] == 1.0 and np.array_equal(acc[t, h, 0], v7)
+            assert np.isneginf(mx[t, h, 1]) and sm[t, h, 1] == 0.0 and not acc[t, h, 1].any()
+    S, tile = 3, 16
+    seg_acc, seg_mx, seg_sm = oracle.segment_partials(ind, row_len, q, pool, 1.0, SM, bt, bs, S, tile)
+    pr = np.zeros((2, 1, S, 2), np.int64)
+    for b in range(2):
+        gl = int(max(row_len[ind[b]:ind[b + 1]]))
+        tps = -(-gl // (S * tile))
+        for s_ in range(S):
+            pr[b, 0, s_] = [s_ * tps * tile, (s_ + 1) * tps * tile]
+    acc2, mx2, sm2 = oracle.range_partials(ind, row_len, q, pool, 1.0, SM, bt, bs, pr)
+    assert np.array_equal(acc2, seg_acc) and np.array_equal(mx2, seg_mx) and np.array_equal(sm2, seg_sm)
+
+
 def test_merge_identity_and_arbitrary_split():
     rng = np.random.default_rng(9)
     L = 57
