@@ -218,6 +218,47 @@ def test_balanced_split_slots_and_merge(S):
     assert_close(torch.tensor(mo), torch.tensor(ml), ref_o, ref_l, f"merged kernel partials, S={S}")
 
 
+@pytest.mark.parametrize("S", [3, 16])
+def test_balanced_parts_match_oracle_slot_by_slot(S):
+    """Every part of the balanced split against the oracle's partial over the
+    part's token range (the rule restated above): same empty slots, the
+    normalised part output to the output tolerance, the part's log-sum-exp to
+    the LSE tolerance."""
+    wl = workloads.verify_mtp4_bf16(seed=14, batch=6, lo=40, hi=3000, num_segments=S)
+    out, lse, step = run_gpu(wl)
+    assert mla.get_device_error() == 0
+    H, B, Q = wl.num_heads, wl.num_reqs, int(wl.qlens.max())
+    RB = mla.row_blocks(Q, H)
+    segm_out, segm_max, segm_sum = mla.workspace_views(step.workspace, B, Q, wl.num_rows, H, S)
+    row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
+    ind = wl.qo_indptr
+    units = []
+    for b in range(B):
+        ln = int(max(row_len[ind[b]:ind[b + 1]]))
+        rows = (ind[b + 1] - ind[b]) * H
+        units += [(-(-ln // 64)) if rb * 64 < rows else 0 for rb in range(RB)]
+    grid = min(torch.cuda.get_device_properties(0).multi_processor_count, B * RB * S)
+    parts = balanced_parts(units, S, grid)
+    ranges = np.zeros((B, RB, S, 2), np.int64)
+    for b in range(B):
+        for rb in range(RB):
+            for s_, (lo, hi) in enumerate(parts[b * RB + rb]):
+                ranges[b, rb, s_] = [lo * 64, hi * 64]
+    acc, mx, sm = oracle.range_partials(ind, row_len, wl.q_bits(), wl.kv_host(), wl.kv_scale, wl.sm_scale,
+                                        wl.block_tables[0], wl.block_size, ranges)
+    gm, gs = segm_max.cpu().numpy(), segm_sum.cpu().numpy()
+    go = blocks_to_rows(segm_out.float().cpu().numpy(), ind, H, wl.num_rows)
+    live = sm > 0
+    assert (np.isneginf(gm) == ~live).all(), "GPU and oracle disagree on which parts are empty"
+    norm_ref = acc[live] / sm[live][:, None]
+    norm_gpu = go[live] / gs[live][:, None]
+    scale = np.abs(norm_ref).max(axis=-1)
+    assert (np.abs(norm_gpu - norm_ref).max(axis=-1) / scale).max() <= 1e-2
+    lse2_ref = mx[live] + np.log2(sm[live])
+    lse2_gpu = gm[live] + np.log2(gs[live])
+    assert np.abs(lse2_gpu - lse2_ref).max() * math.log(2) <= 1e-3
+
+
 @pytest.mark.parametrize("uniform", [False, True])
 def test_poisoned_workspace_is_never_read(uniform):
     """Every segment slot the merge reads is written by the call: a workspace
