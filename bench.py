@@ -1,18 +1,24 @@
 #!/usr/bin/env python3
 """Benchmark of the MLA decode / causal-verify hot path on GB300.
 
-One step = the whole path over one batch: row plan + sub-page expansion
-(mla_plan_rows), split-K decode (mla_decode_verify's decode kernel) and the
-segment merge into bf16 out + natural-log LSE.  Default workload: causal MTP
-verify, qlen 4, bf16 cache, batch 32, 16 heads, seq_len U{1k..8k}, block 64,
-16 split-K segments (seeded synthetic data).
+One step = the whole path over one batch.  Default workload: the simulated
+8-way round-robin context-sharded verify (batch 16, 16 heads, qlen 4, context
+131072, bf16 cache, block 64): mla_plan_rows (global windows) -> the 8 shard
+row views with their sub-page tables (one mla_shard_row_views launch) -> one
+mla_decode_verify launch over the 8 views (balanced split-K) -> segment
+merge into the 8 shard states -> cross-shard natural-log LSE merge into bf16
+out + LSE.
 
-Metric: KV-read GB/s = unique visible latent bytes (sum over requests of the
-longest row's window x 1152 B) / step time, plus query rows / s.  Inputs are
-resident in HBM; L2 is flushed (256 MiB write) before every timed step and the
-flush is outside each step's CUDA-event bracket; the step is one CUDA graph.
+Metric: KV-read GB/s = unique visible latent bytes (every position of every
+request once, 1152 B bf16 / 576 B fp8) / step time, plus query rows / s.
+Inputs are resident in HBM; L2 is flushed (256 MiB write) before every timed
+step, outside each step's CUDA-event bracket; the step is one CUDA graph.
+The same line carries, under "workloads", the other two bandwidth configs
+(qlen-4 verify over 1k-8k contexts; fp8 e4m3 cache with mixed qlen), each
+timed the same way, and under "merge" the merge kernels against HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload dcp8|verify_mtp4|fp8_mixed|decode_qlen1]
 
 N > 1 (under torchrun): every rank runs an independent replica (weak scaling:
 requests are independent, no collective on the data path); value = all
@@ -24,7 +30,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import subprocess
 import sys
@@ -39,29 +44,33 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode/verify KV-read GB/s (% of GB300 HBM peak) and query-rows/sec"
 L2_FLUSH_BYTES = 256 << 20
+WORKLOADS = ["dcp8", "verify_mtp4", "fp8_mixed", "decode_qlen1"]
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="verify_mtp4",
-                    choices=["verify_mtp4", "fp8_mixed", "dcp8", "decode_qlen1"])
+    ap.add_argument("--workload", default="dcp8", choices=WORKLOADS)
+    ap.add_argument("--extra", default="verify_mtp4,fp8_mixed",
+                    help="comma-separated workloads also timed into the line ('none': skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-merge", action="store_true", help="skip the bandwidth-sized merge leg")
+    ap.add_argument("--no-fused", action="store_true", help="skip the in-kernel merge comparison")
     return ap.parse_args()
 
 
 def make_workload(name, seed, device=None):
     from mla_decode_speculative_gb300 import workloads
     if name == "verify_mtp4":
-        return workloads.verify_mtp4_bf16(seed=seed)
+        return workloads.verify_mtp4_bf16(seed=seed, device=device)
     if name == "fp8_mixed":
-        return workloads.fp8_mixed_qlen(seed=seed)
+        return workloads.fp8_mixed_qlen(seed=seed, device=device)
     if name == "dcp8":
         return workloads.dcp8_verify_bf16(seed=seed, device=device)
     return workloads.decode_qlen1_bf16(seed=seed)
@@ -69,16 +78,16 @@ def make_workload(name, seed, device=None):
 
 def kv_bytes(wl) -> int:
     """Unique visible latent bytes of one step: each request's longest row sees
-    its whole seq_len; W shards together hold every position once."""
+    its whole seq_len; the W shards together hold every position once."""
     per_tok = 576 if wl.kv_dtype == "fp8" else 1152
     return int(wl.seq_lens.astype(np.int64).sum()) * per_tok
 
 
 def _balanced_parts(unit_tiles, S, grid):
-    """Tile ranges of the balanced split's parts, per unit (the rule of
-    MLA_DECODE_UNIFORM_SEGMENTS's default in the C header): the units' T tiles
-    end to end, n = min(grid, T // ceil(tmax / (S-1))) chunks
-    [floor(cT/n), floor((c+1)T/n)); a unit's part in chunk c is one segment."""
+    """Tile ranges of the balanced split's parts, per unit (the default split of
+    mla_decode_verify as its header states it): the units' T tiles end to end,
+    n = min(grid, T // ceil(tmax / (S-1))) chunks [floor(cT/n), floor((c+1)T/n));
+    a unit's part in chunk c is one segment."""
     T, tmax = int(sum(unit_tiles)), int(max(unit_tiles))
     need = max(-(-tmax // (S - 1)), 1)
     n = min(grid, max(T // need, 1)) if T else 1
@@ -86,69 +95,137 @@ def _balanced_parts(unit_tiles, S, grid):
     parts, start = [], 0
     for t in unit_tiles:
         t = int(t)
-        c0 = next((c for c in range(n) if bounds[c + 1] > start), n) if t else n
         lst = []
-        c = c0
-        while t and c < n and bounds[c] < start + t:
-            lst.append((max(bounds[c], start) - start, min(bounds[c + 1], start + t) - start))
-            c += 1
+        if t:
+            c = next(c for c in range(n) if bounds[c + 1] > start)
+            while c < n and bounds[c] < start + t:
+                lst.append((max(bounds[c], start) - start, min(bounds[c + 1], start + t) - start))
+                c += 1
         parts.append(lst)
         start += t
     return parts
 
 
-def decode_unit_bytes(wl, grid=None) -> dict:
-    """Algorithmic bytes of one launch of the decode kernel (all shard views
-    of a sharded step in the one launch): visible KV rows, the query rows
-    (once per view), and the split-K partials it must write (an (m, l) pair
-    for every (view, row, head, segment slot), a 1 KiB bf16 vector for every
-    (row, head, part) that holds a visible token).  Parts follow the split
-    the call takes: balanced (S > 1, at most 1024 (view, request, row block)
-    units; grid = the launch's CTAs) or the pages' equal split."""
+def _local(w, r, W, I):
+    """Positions of a window of w that shard r of W holds (runs of I dealt in turn)."""
+    rem = min(max(w % (I * W) - r * I, 0), I)
+    return (w // (I * W)) * I + rem
+
+
+def is_balanced(wl, uniform=False):
+    """Whether mla_decode_verify takes the balanced split for this workload
+    (S > 1, at most 1024 (view, request, row block) units, tile counts within
+    int32), which MLA_DECODE_FUSED_MERGE needs."""
+    P = min(128, wl.block_size & -wl.block_size)
+    S = wl.num_segments
+    W, B, H = wl.world_size, wl.num_reqs, wl.num_heads
+    RB = -(-int(max(wl.qlens)) * H // 64)
+    max_len = max(1, -(-int(wl.max_kv_len) // P)) * P  # the static bound the step passes
+    return (not uniform and S > 1 and W * B * RB <= 1024
+            and W * B * RB * -(-max_len // 64) <= 2 ** 31 - 1)
+
+
+def balanced_units(wl, grid=None):
+    """Per (view, request, row block) unit of the balanced split: (rows of the
+    unit with their visible lengths, the unit's parts as tile ranges)."""
+    S = wl.num_segments
+    W, I, H, B = wl.world_size, wl.interleave, wl.num_heads, wl.num_reqs
+    RB = -(-int(max(wl.qlens)) * H // 64)
+    if grid is None:
+        grid = torch.cuda.get_device_properties(0).multi_processor_count
+    grid = min(grid, W * B * RB * S)
+    tiles, rows = [], []
+    for r in range(W):
+        for b in range(B):
+            L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
+            lens = [_local(L - ql + 1 + t, r, W, I) for t in range(ql)]
+            for rb in range(RB):
+                rl = [lens[(rb * 64 + i) // H] for i in range(64) if rb * 64 + i < ql * H]
+                rows.append(rl)
+                tiles.append(-(-max(lens) // 64) if rl else 0)
+    return list(zip(rows, _balanced_parts(tiles, S, grid)))
+
+
+def split_parts(wl, grid=None, uniform=False):
+    """(active, S, balanced): active = (view, row, head, part) triples whose part
+    holds at least one visible token of that row, under the split the call takes."""
     P = min(128, wl.block_size & -wl.block_size)
     S = wl.num_segments
     W, I, H, B = wl.world_size, wl.interleave, wl.num_heads, wl.num_reqs
-
-    def local(w, r):  # positions of a window of w that shard r holds (runs of I dealt in turn)
-        rem = min(max(w % (I * W) - r * I, 0), I)
-        return (w // (I * W)) * I + rem
-
-    RB = -(-int(max(wl.qlens)) * H // 64)
-    max_len = max(1, -(-int(wl.max_kv_len) // P)) * P  # the static bound the step passes
-    balanced = S > 1 and W * B * RB <= 1024 and W * B * RB * -(-max_len // 64) <= 2 ** 31 - 1
+    balanced = is_balanced(wl, uniform)
     active = 0
+    if S == 1:
+        return 0, 1, False
     if balanced:
-        if grid is None:
-            import torch
-            grid = torch.cuda.get_device_properties(0).multi_processor_count
-        grid = min(grid, W * B * RB * S)
-        units = []
-        for r in range(W):
-            for b in range(B):
-                L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
-                ln = max(local(L - ql + 1 + t, r) for t in range(ql))
-                units += [-(-ln // 64) if rb * 64 < ql * H else 0 for rb in range(RB)]
-        parts = _balanced_parts(units, S, grid)
-        for r in range(W):
-            for b in range(B):
-                L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
-                for t in range(ql):
-                    w = local(L - ql + 1 + t, r)
-                    for h in range(H):
-                        pl = parts[(r * B + b) * RB + (t * H + h) // 64]
-                        active += sum(1 for lo, _ in pl if lo * 64 < w)
+        for rl, pl in balanced_units(wl, grid):
+            active += sum(1 for w in rl for lo, _ in pl if lo * 64 < w)
     else:
         for r in range(W):
             for b in range(B):
                 L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
-                tps_tok = max(1, -(-local(L, r) // (S * P))) * P
+                ln = max(_local(L - ql + 1 + t, r, W, I) for t in range(ql))
+                seg_tok = max(1, -(-ln // (S * P))) * P
                 for t in range(ql):
-                    active += -(-local(L - ql + 1 + t, r) // tps_tok) * H
+                    active += -(-_local(L - ql + 1 + t, r, W, I) // seg_tok) * H
+    return active, S, balanced
+
+
+def decode_unit_bytes(wl, grid=None, uniform=False) -> dict:
+    """Algorithmic bytes of one launch of the decode kernel (all shard views of
+    a sharded step in the one launch): the visible KV rows, the query rows
+    (once per view), and what the split writes -- an (m, l) pair for every
+    (view, row, head, segment slot) and a 1 KiB bf16 vector for every
+    (view, row, head, part) that holds a visible token; with one segment the
+    bf16 output row + LSE of every (view, row, head)."""
+    W, H = wl.world_size, wl.num_heads
+    active, S, _ = split_parts(wl, grid, uniform)
     kv = kv_bytes(wl)
-    q = W * wl.num_rows * H * 1152  # each shard view reads the queries
+    q = W * wl.num_rows * H * 1152
     partial = (W * wl.num_rows * H * S * 8 + active * 1024) if S > 1 else \
         W * wl.num_rows * H * (1024 + 4)
     return {"kv": kv, "q": q, "partials": partial, "total": kv + q + partial}
+
+
+def fused_decode_bytes(wl, grid=None) -> dict:
+    """Algorithmic bytes of one launch of the decode kernel that also merges
+    its split-K parts (MLA_DECODE_FUSED_MERGE): the visible KV rows, the
+    query rows (once per view), every (view, row, head)'s bf16 output row and
+    float32 LSE, and for the units cut into two or more parts the partials
+    written and read back once -- a 1 KiB bf16 vector per (row, head, part)
+    with a visible token, the (m, l) pairs of all S slots written (8 B each)
+    and those of the unit's parts read."""
+    W, H, S = wl.world_size, wl.num_heads, wl.num_segments
+    kv = kv_bytes(wl)
+    q = W * wl.num_rows * H * 1152
+    out = W * wl.num_rows * H * (1024 + 4)
+    partial = 0
+    for rl, pl in balanced_units(wl, grid):
+        if len(pl) < 2:
+            continue
+        act = sum(1 for w in rl for lo, _ in pl if lo * 64 < w)
+        partial += 2 * act * 1024 + len(rl) * (S + len(pl)) * 8
+    return {"kv": kv, "q": q, "out": out, "partials": partial, "total": kv + q + out + partial}
+
+
+def segment_merge_bytes(wl, grid=None, uniform=False) -> dict:
+    """Algorithmic bytes of the segment merge: the live partial vectors (1 KiB
+    bf16 per (view, row, head, part) with a token) and every slot's (m, l)
+    pair read, the bf16 output row and float32 LSE of every (view, row, head)
+    written."""
+    W, H = wl.world_size, wl.num_heads
+    active, S, _ = split_parts(wl, grid, uniform)
+    rd = active * 1024 + W * wl.num_rows * H * S * 8
+    wr = W * wl.num_rows * H * (1024 + 4)
+    return {"read": rd, "write": wr, "total": rd + wr, "live_parts": active}
+
+
+def state_merge_bytes(wl) -> dict:
+    """Algorithmic bytes of the cross-shard merge: W bf16 states + LSEs read per
+    (row, head) (every shard of these long windows is non-empty), one written."""
+    n = wl.num_rows * wl.num_heads
+    rd = wl.world_size * n * (1024 + 4)
+    wr = n * (1024 + 4)
+    return {"read": rd, "write": wr, "total": rd + wr}
 
 
 class ClockSampler:
@@ -158,7 +235,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index):
         self.samples = []
         self.proc = None
         self.index = index
@@ -218,6 +295,32 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(win), "window": window}
 
 
+# ----------------------------------------------------------------------------
+# the float64 oracle on the host cores (cpu_baseline leg and --impl reference)
+
+def _oracle_attention(wl, row_len, q, kv, ind, sel=None, nreq=None):
+    """The oracle over requests [0, nreq) (or the (row, head) pairs sel): plain
+    attention for an unsharded workload; for a context-sharded one the pages'
+    row view [vLLM #51705, 实现拆解 2] -- every shard attends its positions of
+    each row's global window through its own block table, then the shard
+    states are merged -- exactly as the GPU step does it."""
+    import oracle
+    if nreq is not None:
+        ind = ind[:nreq + 1]
+        rows = int(ind[-1])
+        row_len, q = row_len[:rows], q[:rows]
+        tables = wl.block_tables[:, :nreq]
+    else:
+        tables = wl.block_tables
+    if wl.world_size == 1:
+        return oracle.attention(ind, row_len, q, kv, wl.kv_scale, wl.sm_scale, tables[0],
+                                wl.block_size, sel=sel)
+    out, lse, _, _ = oracle.sharded_attention(ind, row_len, q, kv, wl.kv_scale, wl.sm_scale, tables,
+                                              wl.block_size, wl.world_size, sel=sel,
+                                              interleave=wl.interleave)
+    return out, lse
+
+
 def oracle_cpu_baseline(wl, target_s: float):
     """Times the float64 oracle (as it stands) on a prefix of whole requests
     sized to about target_s seconds of host CPU work."""
@@ -225,29 +328,29 @@ def oracle_cpu_baseline(wl, target_s: float):
     oracle.build()
     q = wl.q_bits()
     kv = wl.kv_host()
-    row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
+    ind = wl.qo_indptr
+    row_len, _, _ = oracle.plan_rows(wl.seq_lens, ind)
 
     def run(nreq):
-        ind = wl.qo_indptr[:nreq + 1]
         t0 = time.perf_counter()
-        oracle.attention(ind, row_len[:ind[-1]], q[:ind[-1]], kv, wl.kv_scale, wl.sm_scale,
-                         wl.block_tables[0], wl.block_size)
+        _oracle_attention(wl, row_len, q, kv, ind, nreq=nreq)
         return time.perf_counter() - t0
 
     t1 = run(1)
     per_tok = 576 if wl.kv_dtype == "fp8" else 1152
     L0 = int(wl.seq_lens[0])
-    est = t1 / max(L0, 1)  # seconds per visible token-request
+    est = t1 / max(L0, 1)  # seconds per visible position of a request
     n, acc = 1, L0
     while n < wl.num_reqs and (acc + int(wl.seq_lens[n])) * est <= target_s:
         acc += int(wl.seq_lens[n])
         n += 1
     t = run(n)
     nb = int(wl.seq_lens[:n].astype(np.int64).sum()) * per_tok
-    rows = int(wl.qo_indptr[n])
+    rows = int(ind[n])
+    how = (f"{wl.world_size} shard row views + state merge, " if wl.world_size > 1 else "")
     return {"value": nb / t / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"first {n} of {wl.num_reqs} requests ({rows} verify rows x "
-                      f"{wl.num_heads} heads, {nb / 1e6:.1f} MB of visible KV), {t:.2f} s",
+            "sample": f"first {n} of {wl.num_reqs} requests ({rows} verify rows x {wl.num_heads} heads, "
+                      f"{how}{nb / 1e6:.1f} MB of visible KV), {t:.2f} s",
             "query_rows_per_s": rows / t}
 
 
@@ -261,19 +364,18 @@ def run_reference(args):
     wl = make_workload(args.workload, 0)
     q = wl.q_bits()
     kv = wl.kv_host()
-    row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
+    ind = wl.qo_indptr
+    row_len, _, _ = oracle.plan_rows(wl.seq_lens, ind)
     H = wl.num_heads
     per_tok = 576 if wl.kv_dtype == "fp8" else 1152
-    # each (row, head) item is charged its request's unique KV bytes / (rows x heads)
-    items = [(r, h) for r in range(wl.num_rows) for h in range(H)]
-    req = np.searchsorted(wl.qo_indptr, np.arange(wl.num_rows), side="right") - 1
+    # each (row, head) pair is charged its request's unique KV bytes / (rows x heads)
+    items = np.array([(r, h) for r in range(wl.num_rows) for h in range(H)], np.int32)
+    req = np.searchsorted(ind, np.arange(wl.num_rows), side="right") - 1
     charge = np.array([wl.seq_lens[req[r]] * per_tok / (wl.qlens[req[r]] * H) for r, _ in items])
     budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
-    # calibrate items per step
-    probe = np.array(items[:16], np.int32)
+    probe = items[:16]
     t0 = time.perf_counter()
-    oracle.attention(wl.qo_indptr, row_len, q, kv, wl.kv_scale, wl.sm_scale, wl.block_tables[0],
-                     wl.block_size, sel=probe)
+    _oracle_attention(wl, row_len, q, kv, ind, sel=probe)
     per_item = (time.perf_counter() - t0) / len(probe)
     k = max(1, min(len(items), int(budget / max(per_item, 1e-9))))
     rng = np.random.default_rng(0)
@@ -283,19 +385,19 @@ def run_reference(args):
     for step in range(args.warmup + args.steps):
         idx = order[np.arange(pos, pos + k) % len(items)]
         pos += k
-        sel = np.array([items[i] for i in idx], np.int32)
         t0 = time.perf_counter()
-        oracle.attention(wl.qo_indptr, row_len, q, kv, wl.kv_scale, wl.sm_scale,
-                         wl.block_tables[0], wl.block_size, sel=sel)
+        _oracle_attention(wl, row_len, q, kv, ind, sel=items[idx])
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             tot_t += dt
             tot_b += float(charge[idx].sum())
             tot_rows += k / H
     value = tot_b / tot_t / 1e9
+    how = (f"through the {wl.world_size} shard row views and the state merge"
+           if wl.world_size > 1 else "")
     cpu = {"kind": "oracle", "cores": oracle.num_threads(), "value": value, "unit": "GB/s",
-           "sample": f"{k} (row, head) items per step drawn from the workload, each charged its "
-                     f"request's visible KV bytes / (rows x heads)"}
+           "sample": f"{k} (row, head) pairs per step drawn from the workload {how}, each charged "
+                     f"its request's visible KV bytes / (rows x heads)"}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -306,12 +408,29 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------------------
+
 def source_hash() -> str:
     h = hashlib.sha256()
     for f in ("mla_decode.cu", "mla_ptx.cuh"):
         with open(os.path.join(ROOT, "mla_decode_speculative_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """dram read + write bytes of one launch from the committed ncu summary, when
+    it was taken on this kernel source and workload (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
+            tr = json.load(f)
+        for ent in tr.get("entries", [tr]):
+            if (ent.get("kernel_source_sha256") == source_hash() and ent.get("workload") == workload
+                    and ent.get("kernel", kernel) == kernel):
+                return ent.get("bytes_per_launch")
+    except (OSError, ValueError, AttributeError):
+        pass
+    return None
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -331,6 +450,237 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
+class Timer:
+    """CUDA-event timing of graph replays on one stream, L2 flushed (a 256 MiB
+    write) before every replay, outside the bracket."""
+
+    def __init__(self, stream, device):
+        self.stream = stream
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self, g, n):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        with torch.cuda.stream(self.stream):
+            for k in range(n):
+                # a ~50 us device spin ahead of the flush keeps the launch queue
+                # ahead of the GPU, so no host-side delay falls inside a bracket
+                torch.cuda._sleep(100000)
+                self.flush.zero_()
+                starts[k].record(self.stream)
+                g.replay()
+                ends[k].record(self.stream)
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def capture(stream, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def launches_per_step(wl, fused=False) -> int:
+    """Library kernels one step launches: plan (1), the shard row views
+    (sharded: one launch for all W), decode (1), segment merge (1 if S > 1,
+    unless the decode merges its parts itself), state merge (sharded)."""
+    seg = 1 if wl.num_segments > 1 and not fused else 0
+    if wl.world_size == 1:
+        return 2 + seg
+    return 1 + 1 + 1 + seg + 1
+
+
+class StepBench:
+    """One workload's step, its graphs (whole step, decode alone, merges alone)
+    and their timings.  fused: the decode merges its split-K parts itself
+    (MLA_DECODE_FUSED_MERGE) instead of the separate segment merge."""
+
+    def __init__(self, wl, dev, stream, timer, fused=False):
+        from mla_decode_speculative_gb300 import mla, runner
+        self.wl, self.dev, self.stream, self.timer = wl, dev, stream, timer
+        self.mla = mla
+        self.step = runner.step_for_workload(wl, dev, fused_merge=fused)
+        self.inputs = runner.device_inputs(wl, dev)
+        st = self.step
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                self.run()
+        torch.cuda.synchronize()
+        code = mla.get_device_error()
+        if code:
+            raise RuntimeError(f"device error {mla.DEVICE_ERRORS.get(code, code)} during warm-up")
+        self.graph = capture(stream, self.run)
+        # the row plan / shard views of the warm-up steps stay in the step's buffers
+        q, kv, seq, ind, bt = self.inputs
+        W, Q = wl.world_size, st.max_qlen
+        self.dgraph = self.mgraph = self.sgraph = None
+        # the decode call exactly as the step makes it (a segment merge launch
+        # follows unless the decode merges its parts itself)
+        self.fused = fused
+        skip = wl.num_segments > 1 and not self.fused
+        if W == 1:
+            dec = lambda: mla.decode_verify(q, kv, ind, st.row_len, st.subpage[0], st.P, st.S, Q,
+                                            wl.sm_scale, wl.kv_scale, out=st.out, lse=st.lse,
+                                            workspace=st.workspace, skip_merge=skip, fused_merge=fused)
+            mout, mlse = st.out, st.lse
+        else:
+            dec = lambda: mla.decode_verify(q, kv, ind, st.row_len_local, st.subpage, st.P, st.S, Q,
+                                            wl.sm_scale, wl.kv_scale, out=st.part_out,
+                                            lse=st.part_lse, workspace=st.workspace,
+                                            skip_merge=skip, num_views=W, fused_merge=fused)
+            mout, mlse = st.part_out, st.part_lse
+        self.dgraph = capture(stream, dec)
+        if skip:
+            so, sm, ss = mla.workspace_views(st.workspace, wl.num_reqs, Q, wl.num_rows, wl.num_heads,
+                                             st.S, num_views=W)
+            self.mgraph = capture(stream, lambda: mla.merge_segments(so, sm, ss, ind, Q, out=mout,
+                                                                     lse=mlse, num_views=W))
+        if W > 1:
+            self.sgraph = capture(stream, lambda: mla.merge_states(st.part_out, st.part_lse,
+                                                                   out=st.out, lse=st.lse))
+
+    def run(self):
+        q, kv, seq, ind, bt = self.inputs
+        return self.step(q, kv, seq, ind, bt, self.wl.sm_scale, self.wl.kv_scale)
+
+    def parts(self, n):
+        """Mean ms of the decode alone, the segment merge alone and the state
+        merge alone (each graph replayed with its inputs in place)."""
+        r = {}
+        for key, g in (("decode", self.dgraph), ("segment_merge", self.mgraph),
+                       ("state_merge", self.sgraph)):
+            if g is not None:
+                r[key] = float(np.mean(self.timer(g, n)))
+        return r
+
+    def summary(self, step_ms, parts, peaks, peak_kind):
+        """The per-workload figures: KV GB/s of the step, the decode kernel's
+        roofline, the merges' bandwidth."""
+        wl = self.wl
+        kvb = kv_bytes(wl)
+        hbm = peaks["hbm_gbs"]
+        res = {"workload": wl.name, "ms_per_step": step_ms,
+               "kv_gbs": kvb / (step_ms * 1e-3) / 1e9,
+               "hbm_frac_of_measured": kvb / (step_ms * 1e-3) / 1e9 / hbm,
+               "query_rows_per_s": wl.num_rows / (step_ms * 1e-3),
+               "head_rows_per_s": wl.num_rows * wl.num_heads / (step_ms * 1e-3),
+               "launches_per_step": launches_per_step(wl, self.fused)}
+        if "decode" in parts:
+            ub = fused_decode_bytes(wl) if self.fused else decode_unit_bytes(wl)
+            dms = parts["decode"]
+            kname = "mla_decode_kernel<bf16>" if wl.kv_dtype == "bf16" else "mla_decode_kernel<fp8>"
+            achieved = ub["total"] / (dms * 1e-3) / 1e9
+            res["roofline"] = {
+                "kernel": kname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                "traffic": recorded_traffic(kname, wl.name), "algorithmic_bytes": ub,
+                "avg_launch_ms": dms, "kv_only_gbs": ub["kv"] / (dms * 1e-3) / 1e9,
+                "kv_only_frac": ub["kv"] / (dms * 1e-3) / 1e9 / hbm}
+        merges = {}
+        if "segment_merge" in parts:
+            mb = segment_merge_bytes(wl)
+            ms = parts["segment_merge"]
+            merges["segment_merge"] = {"kernel": "merge_segment_blocks", "bytes": mb, "avg_launch_ms": ms,
+                                       "gbs": mb["total"] / (ms * 1e-3) / 1e9,
+                                       "frac": mb["total"] / (ms * 1e-3) / 1e9 / hbm}
+        if "state_merge" in parts:
+            mb = state_merge_bytes(wl)
+            ms = parts["state_merge"]
+            merges["state_merge"] = {"kernel": "merge_states_small", "bytes": mb, "avg_launch_ms": ms,
+                                     "gbs": mb["total"] / (ms * 1e-3) / 1e9,
+                                     "frac": mb["total"] / (ms * 1e-3) / 1e9 / hbm}
+        if merges:
+            res["merges"] = merges
+        return res
+
+
+def bandwidth_sized_merge(dev, stream, timer, n, peaks):
+    """The segment merge on an instance large enough to be bandwidth-bound: the
+    pages' equal split (16 segments per request, [vLLM #51705, 实现拆解 4]) of a
+    qlen-4 verify batch of 128 requests, 16 heads, seq_len U{1k..8k}; the
+    partials come from a real decode launch and are read from DRAM (L2 flushed
+    before every replay)."""
+    from mla_decode_speculative_gb300 import mla, runner, workloads
+    wl = workloads.verify_mtp4_bf16(seed=5, batch=128, num_segments=16, device=dev)
+    st = runner.step_for_workload(wl, dev, uniform_segments=True)
+    q, kv, seq, ind, bt = runner.device_inputs(wl, dev)
+    with torch.cuda.stream(stream):
+        st(q, kv, seq, ind, bt, wl.sm_scale)
+        mla.decode_verify(q, kv, ind, st.row_len, st.subpage[0], st.P, st.S, st.max_qlen, wl.sm_scale,
+                          out=st.out, lse=st.lse, workspace=st.workspace, skip_merge=True,
+                          uniform_segments=True)
+    torch.cuda.synchronize()
+    so, sm, ss = mla.workspace_views(st.workspace, wl.num_reqs, st.max_qlen, wl.num_rows, wl.num_heads, st.S)
+    g = capture(stream, lambda: mla.merge_segments(so, sm, ss, ind, st.max_qlen, out=st.out, lse=st.lse))
+    ms = float(np.mean(timer(g, n)))
+    mb = segment_merge_bytes(wl, uniform=True)
+    code = mla.get_device_error()
+    if code:
+        raise RuntimeError(f"device error {mla.DEVICE_ERRORS.get(code, code)} in the merge leg")
+    gbs = mb["total"] / (ms * 1e-3) / 1e9
+    return {"kernel": "merge_segment_blocks", "workload": wl.name + "_uniform_split",
+            "bytes": mb, "avg_launch_ms": ms, "gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+            "l2": "flushed before every launch (partials read from DRAM)"}
+
+
+def e2e_leg(sb, dev, stream, world, dist):
+    """The same metric end to end through the public API: each step copies its
+    inputs (q, seq_lens, qo_indptr, block tables) from pinned host memory,
+    runs the step's library calls and copies out + LSE back to pinned host
+    memory; the copies and the calls are captured as one CUDA graph, replayed
+    and synchronised once per step.  The KV cache stays resident on the device
+    (it is the server's state, not a step input)."""
+    wl, st = sb.wl, sb.step
+    h_q = wl.q.pin_memory()
+    h_seq = torch.as_tensor(wl.seq_lens, dtype=torch.int32).pin_memory()
+    h_ind = torch.as_tensor(wl.qo_indptr, dtype=torch.int32).pin_memory()
+    h_bt = torch.as_tensor(wl.block_tables, dtype=torch.int32).pin_memory()
+    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h_lse = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
+    d_q, d_seq, d_ind, d_bt = (torch.empty_like(x, device=dev) for x in (h_q, h_seq, h_ind, h_bt))
+    kv = sb.inputs[1]
+
+    def api_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_seq.copy_(h_seq, non_blocking=True)
+        d_ind.copy_(h_ind, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        o, l = st(d_q, kv, d_seq, d_ind, d_bt, wl.sm_scale, wl.kv_scale)
+        h_out.copy_(o, non_blocking=True)
+        h_lse.copy_(l, non_blocking=True)
+
+    def run(fn, n):
+        s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for k in range(n + 3):
+                sb.timer.flush.zero_()
+                if k >= 3:
+                    s_ev[k - 3].record(stream)
+                fn()
+                if k >= 3:
+                    e_ev[k - 3].record(stream)
+                stream.synchronize()
+        return float(np.mean([s.elapsed_time(e) for s, e in zip(s_ev, e_ev)]))
+
+    n = 200
+    g = capture(stream, api_step)
+    ms = max_over_ranks(run(g.replay, n), dist, dev)
+    eager_ms = max_over_ranks(run(api_step, n), dist, dev)
+    bi = sum(x.numel() * x.element_size() for x in (h_q, h_seq, h_ind, h_bt))
+    bo = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    kvb = kv_bytes(wl)
+    return {"value": world * kvb / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "path": "runner.VerifyStep (C ABI) with pinned host buffers: H2D copies, the step's "
+                    "library calls and the D2H copies captured as one CUDA graph, one "
+                    "synchronisation per step; KV cache resident on the device",
+            "eager": {"value": world * kvb / (eager_ms * 1e-3) / 1e9, "ms_per_step": eager_ms,
+                      "path": "the same calls issued from Python every step (no graph)"}}
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -345,64 +695,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    from mla_decode_speculative_gb300 import build, mla, runner
+    from mla_decode_speculative_gb300 import build, mla
     build.build()
     dev = torch.device("cuda", local)
-    wl = make_workload(args.workload, seed=rank, device=dev if args.workload == "dcp8" else None)
-    step = runner.step_for_workload(wl, dev)
-    q, kv, seq, ind, bt = runner.device_inputs(wl, dev)
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def one_step():
-        step(q, kv, seq, ind, bt, wl.sm_scale, wl.kv_scale)
-
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            one_step()
-    torch.cuda.synchronize()
-    code = mla.get_device_error()
-    if code:
-        raise RuntimeError(f"device error {mla.DEVICE_ERRORS.get(code, code)} during warm-up")
-
-    # the whole step as one CUDA graph
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        one_step()
-    torch.cuda.synchronize()
-
-    # decode kernel alone (partials only), for the roofline
-    dgraph = None
-    if wl.num_segments > 1:
-        # the row plan / shard views of the warm-up steps stay in the step's buffers
-        W = wl.world_size
-        dgraph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(dgraph, stream=stream):
-            if W == 1:
-                mla.decode_verify(q, kv, ind, step.row_len, step.subpage[0], step.P, step.S,
-                                  step.max_qlen, wl.sm_scale, wl.kv_scale, out=step.out,
-                                  lse=step.lse, workspace=step.workspace, skip_merge=True)
-            else:
-                mla.decode_verify(q, kv, ind, step.row_len_local, step.subpage, step.P, step.S,
-                                  step.max_qlen, wl.sm_scale, wl.kv_scale, out=step.part_out,
-                                  lse=step.part_lse, workspace=step.workspace, skip_merge=True,
-                                  num_views=W)
-        torch.cuda.synchronize()
-
-    def timed(g, n):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        with torch.cuda.stream(stream):
-            for k in range(n):
-                # a ~50 us device spin ahead of the flush keeps the launch queue
-                # ahead of the GPU, so no host-side delay falls inside a bracket
-                torch.cuda._sleep(100000)
-                flush.zero_()
-                starts[k].record(stream)
-                g.replay()
-                ends[k].record(stream)
-        torch.cuda.synchronize()
-        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    timer = Timer(stream, dev)
+    peaks, peak_kind = measured_peaks()
+    wl = make_workload(args.workload, seed=rank, device=dev)
+    sb = StepBench(wl, dev, stream, timer)
 
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -412,109 +712,96 @@ def main():
     sampler.start()
     time.sleep(0.3)
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):  # graph warm-up under the same load
-            flush.zero_()
-            graph.replay()
+        for _ in range(max(3, args.warmup)):  # graph warm-up under the same load
+            timer.flush.zero_()
+            sb.graph.replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    step_ms = timed(graph, args.steps)
+    step_ms = timer(sb.graph, args.steps)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     mean_ms = max_over_ranks(float(np.mean(step_ms)), dist, dev)
-    dec_ms = None
-    if dgraph is not None:
-        dec_ms = float(np.mean(timed(dgraph, max(20, min(args.steps, 500)))))
+    n_parts = max(20, min(args.steps, 500))
+    parts = sb.parts(n_parts)
     clocks = sampler.summary(t_wall0, t_wall1)
-    sampler.stop()
     code = mla.get_device_error()
     if code:
         raise RuntimeError(f"device error {mla.DEVICE_ERRORS.get(code, code)} while timing")
+    head = sb.summary(mean_ms, parts, peaks, peak_kind)
 
-    # end to end through the public API: pinned host inputs in, results out
-    e2e = None
-    if not args.no_e2e:
-        h_q = wl.q.pin_memory()
-        h_seq = torch.as_tensor(wl.seq_lens, dtype=torch.int32).pin_memory()
-        h_ind = torch.as_tensor(wl.qo_indptr, dtype=torch.int32).pin_memory()
-        h_bt = torch.as_tensor(wl.block_tables, dtype=torch.int32).pin_memory()
-        h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-        h_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
-        d_q, d_seq, d_ind, d_bt = (torch.empty_like(x, device=dev) for x in (h_q, h_seq, h_ind, h_bt))
-        n_e2e = max(20, min(args.steps, 300))
-        s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
-        e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    e2e = None if args.no_e2e else e2e_leg(sb, dev, stream, world, dist)
+
+    # the other configured bandwidth workloads, timed the same way
+    extra = {}
+    names = [] if args.extra in ("", "none") else [w for w in args.extra.split(",") if w != args.workload]
+    for name in names:
+        ewl = make_workload(name, seed=rank, device=dev)
+        esb = StepBench(ewl, dev, stream, timer)
         with torch.cuda.stream(stream):
-            for k in range(n_e2e + 3):
-                flush.zero_()
-                if k >= 3:
-                    s_ev[k - 3].record(stream)
-                d_q.copy_(h_q, non_blocking=True)
-                d_seq.copy_(h_seq, non_blocking=True)
-                d_ind.copy_(h_ind, non_blocking=True)
-                d_bt.copy_(h_bt, non_blocking=True)
-                o, l = step(d_q, kv, d_seq, d_ind, d_bt, wl.sm_scale, wl.kv_scale)
-                h_out.copy_(o, non_blocking=True)
-                h_lse.copy_(l, non_blocking=True)
-                if k >= 3:
-                    e_ev[k - 3].record(stream)
-                stream.synchronize()
-        e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(s_ev, e_ev)])),
-                                dist, dev)
-        bi = sum(x.numel() * x.element_size() for x in (h_q, h_seq, h_ind, h_bt))
-        bo = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
-        e2e = {"value": world * kv_bytes(wl) / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "path": "runner.VerifyStep (C ABI, eager) with pinned host buffers; KV cache "
-                       "resident on the device"}
-
-    peaks, peak_kind = measured_peaks()
-    roofline = None
-    if dec_ms is not None:
-        ub = decode_unit_bytes(wl)
-        achieved = ub["total"] / (dec_ms * 1e-3) / 1e9
-        traffic = None
-        try:
-            with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
-                tr = json.load(f)
-            for ent in tr.get("entries", [tr]):
-                if ent.get("kernel_source_sha256") == source_hash() and ent.get("workload") == wl.name:
-                    traffic = ent.get("bytes_per_launch")
-        except (OSError, ValueError, AttributeError):
-            pass
-        roofline = {"kernel": "mla_decode_kernel<bf16>" if wl.kv_dtype == "bf16" else
-                    "mla_decode_kernel<fp8>", "bound": "hbm", "achieved": achieved,
-                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
-                    "traffic": traffic, "algorithmic_bytes": ub,
-                    "avg_launch_ms": dec_ms,
-                    "kv_only_gbs": ub["kv"] / (dec_ms * 1e-3) / 1e9}
+            for _ in range(max(3, args.warmup)):
+                timer.flush.zero_()
+                esb.graph.replay()
+        ems = max_over_ranks(float(np.mean(timer(esb.graph, args.steps))), dist, dev)
+        extra[name] = esb.summary(ems, esb.parts(n_parts), peaks, peak_kind)
+        code = mla.get_device_error()
+        if code:
+            raise RuntimeError(f"device error {mla.DEVICE_ERRORS.get(code, code)} in {name}")
+        del esb, ewl
+        torch.cuda.empty_cache()
+    # the same workloads with the split-K parts merged inside the decode kernel
+    fused_cmp = {}
+    if not args.no_fused:
+        for name in [args.workload] + names:
+            fwl = wl if name == args.workload else make_workload(name, seed=rank, device=dev)
+            if not is_balanced(fwl):
+                continue
+            fsb = StepBench(fwl, dev, stream, timer, fused=True)
+            fms = max_over_ranks(float(np.mean(timer(fsb.graph, min(args.steps, 200)))), dist, dev)
+            fsum = fsb.summary(fms, fsb.parts(min(args.steps, 200)), peaks, peak_kind)
+            sep = head if name == args.workload else extra[name]
+            fused_cmp[name] = {"ms_per_step": fms, "kv_gbs": fsum["kv_gbs"],
+                               "decode_ms": fsum["roofline"]["avg_launch_ms"],
+                               "separate_merge_ms_per_step": sep["ms_per_step"],
+                               "flag": "MLA_DECODE_FUSED_MERGE"}
+            code = mla.get_device_error()
+            if code:
+                raise RuntimeError(f"device error {mla.DEVICE_ERRORS.get(code, code)} in fused {name}")
+            del fsb
+            torch.cuda.empty_cache()
+    merge = dict(head.get("merges", {}))
+    if not args.no_merge:
+        merge["bandwidth_sized"] = bandwidth_sized_merge(dev, stream, timer, n_parts, peaks)
+    clocks_all = sampler.summary(t_wall0, time.time())
+    sampler.stop()
 
     kvb = kv_bytes(wl)
     value = world * kvb / (mean_ms * 1e-3) / 1e9
-    # plan (1) + decode (1) + segment merge (1 if S > 1); sharded: plan + W
-    # shard views + one decode over the W views + segment merge + state merge
-    per_decode = 2 if wl.num_segments > 1 else 1
-    launches_per_step = (1 + per_decode if wl.world_size == 1 else
-                         1 + wl.world_size + per_decode + 1)
+    gpu_launches = launches_per_step(wl) * args.steps
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if wl.kv_dtype == "bf16" else "fp8_e4m3 cache, bf16 MMA",
             "data": "synthetic",
             "config": {**wl.describe(), "parallelism": f"replicas x{world}" if world > 1 else "1 gpu",
+                       "shards": (f"{wl.world_size} round-robin context shards simulated on one GPU "
+                                  "(all shard views in one decode launch, then the state merge)"
+                                  if wl.world_size > 1 else "none"),
                        "l2": "flushed (256 MiB write) before every step, outside the timed bracket",
                        "launch": "one CUDA graph per step", "seed": "rank"},
             "hbm_frac_of_measured": value / world / peaks["hbm_gbs"],
             "query_rows_per_s": world * wl.num_rows / (mean_ms * 1e-3),
             "head_rows_per_s": world * wl.num_rows * wl.num_heads / (mean_ms * 1e-3),
-            "roofline": roofline, "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks, "e2e": e2e}
+            "roofline": head.get("roofline"), "gpu_launches": gpu_launches,
+            "clocks": clocks, "e2e": e2e, "merge": merge or None,
+            "workloads": {k: v for k, v in extra.items()},
+            "fused_merge": fused_cmp or None,
+            "clocks_whole_run": clocks_all}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_cpu_baseline(wl, args.cpu_seconds)
     if rank == 0:

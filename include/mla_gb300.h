@@ -52,7 +52,7 @@ typedef struct CUstream_st *mla_stream_t;
 
 #define MLA_D_QK 576  /* q / K width: 512 latent + 64 rope   */
 #define MLA_D_V 512   /* V / output width: the 512-d latent */
-#define MLA_ABI_VERSION 4
+#define MLA_ABI_VERSION 5
 
 typedef enum mla_status {
   MLA_OK = 0,
@@ -141,6 +141,24 @@ mla_status mla_shard_row_view(int num_reqs, int num_rows,
                               int block_size, int32_t *subpage_table,
                               int subpage_stride, mla_stream_t stream);
 
+/* All world_size shard row views of one step in one launch -- the ranks of a
+ * context-sharded step simulated on one GPU (the pages run one view per
+ * rank).  View r is exactly mla_shard_row_view(rank = r): it reads
+ * block_tables + r * num_reqs * block_table_stride (rank r's own table over
+ * its local tokens, when block_tables != NULL) and writes
+ * row_len_local + r * num_rows and subpage_tables + r * num_reqs *
+ * subpage_stride, i.e. row_len_local [W, T] and subpage_tables [W, B, stride]
+ * as mla_decode_verify's num_views = W reads them.  1 <= world_size <= 65535;
+ * errors and device checks as mla_shard_row_view. */
+mla_status mla_shard_row_views(int num_reqs, int num_rows,
+                               const int32_t *qo_indptr,
+                               const int32_t *row_len_global, int world_size,
+                               int interleave, int32_t *row_len_local,
+                               const int32_t *block_tables,
+                               int block_table_stride, int num_blocks,
+                               int block_size, int32_t *subpage_tables,
+                               int subpage_stride, mla_stream_t stream);
+
 /* Arguments of mla_decode_verify (host struct, read during the call). */
 typedef struct mla_decode_args {
   int num_reqs;          /* B >= 1 */
@@ -171,6 +189,13 @@ typedef struct mla_decode_args {
    * [V, T, H, 512], lse [V, T, H]; no counterpart in the pages, which run one
    * decode per rank. */
   int num_views;
+  /* Bound on every in-kernel wait for the work to progress, in SM clock
+   * cycles; 0 = the default of 4e9 cycles (about 2 s).  A wait that runs out
+   * records MLA_DEV_WAIT_TIMEOUT and the kernel returns without its result
+   * (it first lets its own copies and MMAs in flight finish, under a separate
+   * fixed bound).  Only a caller that wants to exercise that exit path needs
+   * a small value. */
+  int64_t wait_cycles;
 } mla_decode_args;
 
 typedef enum mla_decode_flags {
@@ -192,7 +217,20 @@ typedef enum mla_decode_flags {
    * tokens [s*L, (s+1)*L) with L = ceil(len / (S*P)) * P, len the
    * request's longest visible row.  The merged out / lse are the same either
    * way up to float rounding. */
-  MLA_DECODE_UNIFORM_SEGMENTS = 2
+  MLA_DECODE_UNIFORM_SEGMENTS = 2,
+  /* With the balanced split: merge the split-K parts inside the decode kernel
+   * instead of a separate merge launch.  A unit lying inside one SM's chunk
+   * is written as bf16 out + LSE straight from its accumulator; the parts of
+   * a unit cut across chunks are published to the workspace (a release add
+   * on a per-unit counter), and the SMs holding them merge its 64-dim output
+   * blocks once their own tiles are done (a holder waits, bounded, only when
+   * every chunk of the unit is claimed by a running SM; the last part to
+   * arrive merges whatever no holder claimed).  The result is the same up to
+   * float rounding.  Needs num_segments > 1 and neither flag above
+   * (MLA_ERR_UNSUPPORTED otherwise, or when the call cannot take the
+   * balanced split).  Off by default: on this library's configured workloads
+   * the merge tail inside the kernel measured slower than the separate merge. */
+  MLA_DECODE_FUSED_MERGE = 4
 } mla_decode_flags;
 
 /* Workspace bytes mla_decode_verify needs for `a`.  Layout, each region
@@ -216,12 +254,13 @@ size_t mla_decode_verify_workspace(const mla_decode_args *a);
  *   out[r,h,:] = sum_j softmax(s)_j * k_j[0:512],  lse[r,h] = ln sum_j e^{s_j}
  * [sglang #34432 snippets; vLLM #51705, 实现拆解 2].  Rows of a request are
  * processed jointly against shared KV tiles with per-row causal masks; the
- * rows' lengths may differ by any amount.  With num_segments S > 1 the work
- * of each request is split into S segments of tiles_per_segment =
- * cdiv(len, S * P) pages (len = the request's longest row) whose base-2
- * partial (max, exp2-sum, unnormalised output) are written to the workspace
- * and merged into bf16 out + natural-log LSE by the segment merge
- * [vLLM #51705, 实现拆解 4]; S == 1 writes out/lse directly.
+ * rows' lengths may differ by any amount.  With num_segments S > 1 the KV
+ * tokens of each (view, request, 64-row block) are split into up to S
+ * segment slots -- by default the balanced split, with
+ * MLA_DECODE_UNIFORM_SEGMENTS the pages' equal split (see mla_decode_flags)
+ * -- whose base-2 partials (max, exp2-sum, unnormalised output) go to the
+ * workspace and are merged into bf16 out + natural-log LSE by the segment
+ * merge [vLLM #51705, 实现拆解 4]; S == 1 writes out/lse directly.
  * fp8 codes are converted to bf16 exactly; kv_scale is folded into the score
  * scale and into the output.  The query-by-key products use bf16 tensor-core
  * MMAs with float32 accumulation; softmax probabilities are rounded to bf16
@@ -302,8 +341,7 @@ mla_status mla_write_kv(int num_reqs, int num_rows, const int32_t *seq_lens,
                         int64_t num_cache_rows, mla_stream_t stream);
 
 /* The same decode / verify as mla_decode_verify, for callers that cannot
- * allocate device memory where they make the call -- code running under
- * CUDA-graph capture (cudaMalloc is not allowed there), serving runtimes that
+ * allocate device memory where they make the call -- serving runtimes that
  * reserve all device memory at start-up and forbid allocation on the request
  * path, and plain C or plugin hosts that hold no device allocator (for them a
  * cudaMalloc would also synchronise the device mid-step).  The pages have no

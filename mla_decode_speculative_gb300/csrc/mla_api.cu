@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -17,8 +18,10 @@ namespace mla {
 namespace {
 thread_local char g_last_error[512] = "";
 __device__ int g_device_error;  // first device-detected problem (mla_device_error)
-int *g_err_ptr[64];
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+// Per-device caches filled on first use.  Two host threads may fill one at
+// the same time; both store the same value, so relaxed atomics suffice.
+std::atomic<int *> g_err_ptr[64];
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
 __device__ __forceinline__ void dev_error(int *err, int code) { atomicCAS(err, 0, code); }
 
@@ -127,10 +130,18 @@ __global__ void plan_kernel(int B, int T, const int32_t *seq_lens, const int32_t
 
 // Shard row view: per-row shard-local count from the row's global window;
 // blocks row_blocks + b expand the shard's table for request b, sized by its
-// longest shard-local row.
+// longest shard-local row.  blockIdx.y selects the rank (rank0 + y) when
+// several views are computed in one launch; view y's outputs and block table
+// sit at the given per-view strides.
 __global__ void shard_kernel(int B, int T, const int32_t *ind, const int32_t *row_len_global,
-                             int W, int rank, int I, int32_t *row_len_local, TableArgs tab,
-                             int row_blocks, int *err) {
+                             int W, int rank0, int I, int32_t *row_len_local, TableArgs tab,
+                             int row_blocks, int *err, int64_t bt_view_stride, int64_t sp_view_stride) {
+  const int rank = rank0 + static_cast<int>(blockIdx.y);
+  row_len_local += static_cast<int64_t>(blockIdx.y) * T;
+  if (tab.bt != nullptr) {
+    tab.bt += static_cast<int64_t>(blockIdx.y) * bt_view_stride;
+    tab.sp += static_cast<int64_t>(blockIdx.y) * sp_view_stride;
+  }
   const int total = ind[B];
   const bool ind_ok = ind[0] == 0 && total >= 0 && total <= T;
   if (blockIdx.x >= row_blocks) {
@@ -182,37 +193,47 @@ int *device_error_word() {
     set_error("device ordinal %d out of range", dev);
     return nullptr;
   }
-  if (g_err_ptr[dev] == nullptr) {
+  int *cached = g_err_ptr[dev].load(std::memory_order_relaxed);
+  if (cached == nullptr) {
     void *ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_device_error);
     if (e != cudaSuccess) {
       cuda_fail(e, "cudaGetSymbolAddress(device error word)");
       return nullptr;
     }
-    g_err_ptr[dev] = static_cast<int *>(ptr);
+    cached = static_cast<int *>(ptr);
+    g_err_ptr[dev].store(cached, std::memory_order_relaxed);
   }
-  return g_err_ptr[dev];
+  return cached;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = g_encode.load(std::memory_order_relaxed);
+  if (fn != nullptr) return fn;
+  void *sym = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &sym, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || sym == nullptr) {
+    set_error("cuTensorMapEncodeTiled entry point unavailable");
+    return nullptr;
+  }
+  fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(sym);
+  g_encode.store(fn, std::memory_order_relaxed);
+  return fn;
 }
 
 mla_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
                         int elem_bytes, uint64_t cols, uint64_t rows, uint32_t box_cols,
                         uint32_t box_rows, CUtensorMapSwizzle swizzle) {
-  if (g_encode == nullptr) {
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                     cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
-      set_error("cuTensorMapEncodeTiled entry point unavailable");
-      return MLA_ERR_CUDA;
-    }
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return MLA_ERR_CUDA;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * static_cast<uint64_t>(elem_bytes)};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+  const CUresult r = encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -230,17 +251,14 @@ mla_status make_tmap_tile3d(CUtensorMap *map, const void *base, CUtensorMapDataT
   // chunk) with strides (row = 576 values, chunk = 64 values), so one box of
   // (64, box_rows, 9) lands chunk-major in shared memory: chunk c at
   // c * box_rows * 64 * elem_bytes, rows inside a chunk contiguous.
-  if (g_encode == nullptr) {
-    CUtensorMap scratch;
-    const mla_status st = make_tmap_2d(&scratch, base, dtype, elem_bytes, 576, rows, 64, 8, swizzle);
-    if (st != MLA_OK) return st;
-  }
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return MLA_ERR_CUDA;
   const uint64_t eb = static_cast<uint64_t>(elem_bytes);
   const cuuint64_t dims[3] = {64, rows, 9};
   const cuuint64_t strides[2] = {576 * eb, 64 * eb};
   const cuuint32_t box[3] = {64, box_rows, 9};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+  const CUresult r = encode(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -264,14 +282,15 @@ mla_status launch_plan_rows(int B, int T, const int32_t *seq_lens, const int32_t
 }
 
 mla_status launch_shard_rows(int B, int T, const int32_t *ind, const int32_t *row_len_global,
-                             int W, int rank, int interleave, int32_t *row_len_local,
+                             int W, int rank, int num_views, int interleave, int32_t *row_len_local,
                              const TableLaunch &t, int *err, cudaStream_t stream) {
   const int row_blocks = grid_for(T, 256);
   TableArgs tab{t.block_table, t.bt_stride, t.num_blocks, t.block_size, t.page_size,
                 t.subpage_table, t.sp_stride};
   const int blocks = row_blocks + (t.block_table != nullptr ? B : 0);
-  shard_kernel<<<blocks, 256, 0, stream>>>(B, T, ind, row_len_global, W, rank, interleave,
-                                           row_len_local, tab, row_blocks, err);
+  const int64_t bt_view = static_cast<int64_t>(B) * t.bt_stride, sp_view = static_cast<int64_t>(B) * t.sp_stride;
+  shard_kernel<<<dim3(blocks, num_views), 256, 0, stream>>>(B, T, ind, row_len_global, W, rank, interleave,
+                                                            row_len_local, tab, row_blocks, err, bt_view, sp_view);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "shard_row_view launch");
 }
@@ -292,7 +311,14 @@ WorkspaceLayout decode_workspace_layout(const mla_decode_args &a) {
     off += align256(items * sizeof(float));
   }
   l.sched = off;
-  l.total = off + 256;
+  off += 256;
+  l.unit_state = off;
+  if (a.num_segments > 1) {
+    const size_t V = a.num_views > 1 ? a.num_views : 1;
+    const size_t row_blocks = (static_cast<size_t>(a.max_qlen) * a.num_heads + 63) / 64;
+    off += align256(V * a.num_reqs * row_blocks * sizeof(unsigned));
+  }
+  l.total = off;
   return l;
 }
 
@@ -396,7 +422,37 @@ mla_status mla_shard_row_view(int num_reqs, int num_rows, const int32_t *qo_indp
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   TableLaunch t{block_table, block_table_stride, num_blocks, block_size, P, subpage_table,
                 subpage_stride};
-  return launch_shard_rows(num_reqs, num_rows, qo_indptr, row_len_global, world_size, rank,
+  return launch_shard_rows(num_reqs, num_rows, qo_indptr, row_len_global, world_size, rank, 1,
+                           interleave, row_len_local, t, err, s);
+}
+
+mla_status mla_shard_row_views(int num_reqs, int num_rows, const int32_t *qo_indptr,
+                               const int32_t *row_len_global, int world_size, int interleave,
+                               int32_t *row_len_local, const int32_t *block_tables,
+                               int block_table_stride, int num_blocks, int block_size,
+                               int32_t *subpage_tables, int subpage_stride, mla_stream_t stream) {
+  if (world_size < 1 || world_size > 65535 || interleave < 1 ||
+      static_cast<int64_t>(interleave) * world_size > INT32_MAX) {
+    set_error("mla_shard_row_views: world_size %d, interleave %d", world_size, interleave);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (num_reqs < 0 || num_rows < 0 || qo_indptr == nullptr ||
+      (num_rows > 0 && (row_len_global == nullptr || row_len_local == nullptr))) {
+    set_error("mla_shard_row_views: bad sizes or null pointers (B=%d T=%d)", num_reqs, num_rows);
+    return MLA_ERR_INVALID_ARG;
+  }
+  int P = 0;
+  if (block_tables != nullptr) {
+    mla_status st = check_table_args(block_tables, block_table_stride, num_blocks, block_size,
+                                     subpage_tables, subpage_stride, &P);
+    if (st != MLA_OK) return st;
+  }
+  int *err = device_error_word();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  TableLaunch t{block_tables, block_table_stride, num_blocks, block_size, P, subpage_tables,
+                subpage_stride};
+  return launch_shard_rows(num_reqs, num_rows, qo_indptr, row_len_global, world_size, 0, world_size,
                            interleave, row_len_local, t, err, s);
 }
 
@@ -421,8 +477,17 @@ static mla_status check_decode_args(const mla_decode_args *a) {
     return MLA_ERR_UNSUPPORTED;
   }
   if (static_cast<int64_t>(a->subpage_stride) * a->page_size > INT32_MAX ||
-      a->num_cache_rows > INT32_MAX || static_cast<int64_t>(a->num_rows) * a->num_heads > INT32_MAX) {
+      a->num_cache_rows > INT32_MAX || static_cast<int64_t>(a->num_rows) * a->num_heads > INT32_MAX ||
+      static_cast<int64_t>(a->max_qlen) * a->num_heads > INT32_MAX) {
     set_error("mla_decode_verify: sizes overflow int32 indexing");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (a->max_qlen > a->num_rows) {
+    set_error("mla_decode_verify: max_qlen %d above the row capacity %d", a->max_qlen, a->num_rows);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (a->wait_cycles < 0) {
+    set_error("mla_decode_verify: wait_cycles must be >= 0 (0 = default)");
     return MLA_ERR_INVALID_ARG;
   }
   if (a->num_segments > kMaxParts) {
@@ -443,9 +508,15 @@ static mla_status check_decode_args(const mla_decode_args *a) {
     set_error("mla_decode_verify: num_views %d (rows x heads x views must fit int32)", a->num_views);
     return MLA_ERR_INVALID_ARG;
   }
-  if ((a->flags & ~(MLA_DECODE_SKIP_MERGE | MLA_DECODE_UNIFORM_SEGMENTS)) != 0) {
+  if ((a->flags & ~(MLA_DECODE_SKIP_MERGE | MLA_DECODE_UNIFORM_SEGMENTS | MLA_DECODE_FUSED_MERGE)) != 0) {
     set_error("mla_decode_verify: unknown flags 0x%x", a->flags);
     return MLA_ERR_INVALID_ARG;
+  }
+  if ((a->flags & MLA_DECODE_FUSED_MERGE) &&
+      ((a->flags & (MLA_DECODE_SKIP_MERGE | MLA_DECODE_UNIFORM_SEGMENTS)) || a->num_segments < 2)) {
+    set_error("mla_decode_verify: MLA_DECODE_FUSED_MERGE needs num_segments > 1 and neither "
+              "MLA_DECODE_SKIP_MERGE nor MLA_DECODE_UNIFORM_SEGMENTS");
+    return MLA_ERR_UNSUPPORTED;
   }
   if (!(a->sm_scale > 0.0f) || (a->kv_dtype == MLA_KV_FP8_E4M3 && !(a->kv_scale > 0.0f))) {
     set_error("mla_decode_verify: sm_scale and (fp8) kv_scale must be positive");
@@ -477,14 +548,17 @@ mla_status mla_decode_verify(const mla_decode_args *a, void *workspace, size_t w
   d.a = a;
   d.err = err;
   d.sched = reinterpret_cast<int *>(w + lay.sched);
+  d.unit_state = reinterpret_cast<unsigned *>(w + lay.unit_state);
+  d.state_bytes = lay.total - lay.sched;
   const bool partials = a->num_segments > 1;
   if (partials) {
     d.segm_out = reinterpret_cast<uint16_t *>(w + lay.segm_out);
     d.segm_max = reinterpret_cast<float *>(w + lay.segm_max);
     d.segm_sum = reinterpret_cast<float *>(w + lay.segm_sum);
   }
-  st = launch_decode(d, s);
-  if (st != MLA_OK || !partials || (a->flags & MLA_DECODE_SKIP_MERGE)) return st;
+  bool merged = false;
+  st = launch_decode(d, s, &merged);
+  if (st != MLA_OK || !partials || merged || (a->flags & MLA_DECODE_SKIP_MERGE)) return st;
   MergeLaunch m{};
   m.mode = MLA_MERGE_SEGMENTS;
   m.num_rows = a->num_rows;

@@ -52,6 +52,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -90,11 +91,27 @@ struct WorkEntry {
   int w;          // claim index (item or chunk), -1 = no more work
   int b, rb, seg, q_row, row_base, n_rows, seg_lo, seg_hi, n_tiles;  // b: view * B + request
   int fill_hi;    // segment slots seg+1 .. fill_hi-1 of these rows get no part: mark them empty
+  int unit;       // balanced split: the (view, request, row block) unit of this part
+  int n_parts;    // balanced split: parts the unit has (0: a unit without tiles)
+  int c_last;     // balanced split: chunk holding the unit's last part
   alignas(16) int lens[kRows];  // visible tokens of each of the block's rows (0 past n_rows)
 };
 constexpr int kWorkRing = 4;
 constexpr int kMaxOrderedReqs = 128;  // requests ranked longest-first in every CTA
 constexpr int kMaxUnits = 1024;       // balanced split: (view, request, row block) units tabulated per CTA
+
+// In-kernel split-K merge (balanced split): a part of a multi-part unit that
+// this CTA computed; it is published, and the unit's claimed 64-dim output
+// blocks merged, once the CTA's own work is done.
+struct PendMerge {
+  int b, rb, row_base, n_rows, n_parts, unit;
+  int seg, c_last;  // this part's index in the unit; chunk of the unit's last part
+  unsigned todo;    // bit k: output dims 64k .. 64k + 63 are merged by this CTA
+  int wait;         // 1: wait until every part of the unit is published
+  int go;           // the unit is complete (or this CTA's wait ran out: 0)
+  int staged;       // byte offset of its parts' slices in the staging area, -1: read from L2 directly
+};
+constexpr int kMaxPend = 4;  // one chunk per CTA holds at most two multi-part units
 
 struct Misc {
   uint64_t full[kStages];
@@ -113,6 +130,9 @@ struct Misc {
   int req_order[kMaxOrderedReqs]; // requests, longest first
   int unit_end[kMaxUnits];        // balanced split: tiles of units 0..u (inclusive prefix sum)
   float red[2][2][4][32];  // [buffer][column group][lane quarter][lane]
+  PendMerge pend[kMaxPend];       // softmax warps: merges to run after the CTA's own parts
+  int n_pend;
+  int merge_go;
 };
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc)) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -129,8 +149,10 @@ struct Params {
   float *lse;
   int *err;
   int *sched;              // work-claim counter, zero at launch
+  unsigned *unit_state;    // per unit: parts published (bits 0-15), output blocks claimed by waiting holders (16-23)
   int64_t num_cache_rows;
-  long long wait_budget;
+  long long wait_budget;   // SM cycles any wait on the work may take before the CTA gives up
+  long long drain_budget;  // SM cycles the exit path waits for this CTA's own copies and MMAs
   int subpage_stride;
   int page_size;
   int num_heads;
@@ -144,6 +166,7 @@ struct Params {
   int max_len;
   int tile3d;              // KV tensor map is the 3-D whole-tile view (page size >= 64)
   int balanced;            // split-K by equal chunks of the batch's tiles (else S equal segments per request)
+  int fused;               // balanced split merged in this kernel into out / lse (no merge launch)
   int num_units;           // num_views * num_reqs * row_blocks
   float score_scale_log2;  // sm_scale * kv_scale * log2(e)
   float out_scale;         // kv_scale (fp8) or 1
@@ -213,8 +236,15 @@ __device__ __forceinline__ bool decode_unit(const Params &p, int v, int b, int r
 __device__ __forceinline__ int request_len(const Params &p, int v, int b) {
   const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
   if (q0 < 0 || q1 < q0 || q1 > p.num_rows || q1 - q0 > p.max_qlen) return 0;
+  const int32_t *rl = p.row_len + static_cast<int64_t>(v) * p.num_rows;
   int len = 0;
-  for (int t = q0; t < q1; ++t) len = max(len, min(max(p.row_len[v * p.num_rows + t], 0), p.max_len));
+  for (int t0 = q0; t0 < q1; t0 += 8) {  // eight loads in flight, then the max
+    int l[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) l[k] = t0 + k < q1 ? rl[t0 + k] : 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) len = max(len, min(max(l[k], 0), p.max_len));
+  }
   return len;
 }
 
@@ -280,7 +310,308 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes) {
   return pack_bf16(f.x, f.y);
 }
 
-template <bool kFp8>
+// ---- in-kernel split-K merge (balanced split)
+
+__device__ __forceinline__ int ld_volatile(const int *ptr) {
+  int v;
+  asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *ptr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned atom_add_release_gpu(unsigned *ptr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+  return old;
+}
+
+constexpr uint32_t kMergeBar = 5;                        // named barrier of the 256 softmax threads
+constexpr int kMergeThreads = kNumSoftmaxWarps * 32;
+constexpr int kMergeSlots = 32;                          // parts whose weights are staged at a time
+
+// Shared-memory scratch of one block merge (inside stage 0, free once the
+// CTA's own tiles are done).
+constexpr int kMergePassDims = 128;                     // output dims merged per pass
+struct MergeScratch {
+  float m[kMergeSlots][kRows];         // base-2 max of (part, row), parts 0 .. 31
+  float w[kMergeSlots][kRows];         // normalised weight of (part, row), 32 parts at a time
+  uint16_t o[kRows][kMergePassDims + 8];  // merged bf16 [row][dim] of one pass, padded rows
+  float M[kRows], inv[kRows];          // row max (base 2) and 1 / denominator
+  float part_m[4][kRows], part_d[4][kRows];
+};
+static_assert(sizeof(MergeScratch) <= kStageBytes, "merge scratch fits one stage");
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void *gptr) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+constexpr int kStagingBytes = kStages * kStageBytes;  // the two stages, free once the CTA's tiles are done
+
+// The claimed output dims of a unit as one run of consecutive 64-dim blocks:
+// (first block, number of blocks), or nb = 0 when the claim is not one run.
+__device__ __forceinline__ void todo_run(unsigned todo, int &b0, int &nb) {
+  b0 = __ffs(todo) - 1;
+  nb = __popc(todo);
+  if (((todo >> b0) & ((1u << nb) - 1u)) != ((1u << nb) - 1u)) nb = 0;
+}
+
+// Issues the copies of a staged unit's parts into shared memory: for every
+// part u and row octet o, the claimed dims' 16-byte (8-row) pieces, as
+// [part][octet][dim] (cp.async, 16 bytes per thread and instruction; a warp
+// covers 512 consecutive bytes).
+__device__ void stage_unit(const Params &p, const PendMerge &pm, uint32_t s_stage, int tid) {
+  int b0, nb;
+  todo_run(pm.todo, b0, nb);
+  const int D = 64 * nb, S = p.num_segments;
+  const int64_t blk0 = (static_cast<int64_t>(pm.b) * p.row_blocks + pm.rb) * S;
+  const int total = pm.n_parts * 8 * D;
+  const uint32_t dst0 = s_stage + static_cast<uint32_t>(pm.staged);
+  for (int c = tid; c < total; c += kMergeThreads) {
+    const int d = c % D, uo = c / D;  // uo = part * 8 + octet
+    const int u = uo >> 3, o = uo & 7;
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + u) * (512 * kRows)) + o * 512 + 64 * b0 + d;
+    cp_async16(dst0 + static_cast<uint32_t>(c) * 16u, src);
+  }
+}
+
+// Per-row max and denominator of a unit's n published parts, and the
+// natural-log LSE (written when write_lse): four threads per row, parts
+// strided by 4, a running (max, sum) rescaled as the max grows; the maxima of
+// the first 32 parts stay in shared memory for the weights.
+__device__ void merge_unit_stats(const Params &p, const PendMerge &pm, bool write_lse, int tid, MergeScratch &ms) {
+  const int S = p.num_segments, n = pm.n_parts;
+  const float *mx = p.segm_max + static_cast<int64_t>(pm.row_base) * S;  // [rows][S]
+  const float *sm = p.segm_sum + static_cast<int64_t>(pm.row_base) * S;
+  const int row = tid & (kRows - 1), quarter = tid >> 6;
+  float Mq = -INFINITY, dq = 0.0f;
+  auto take = [&](float m, float l) {
+    if (m == -INFINITY) return;
+    if (m > Mq) {
+      dq = dq * exp2f(Mq - m) + l;  // 0 while Mq is -inf
+      Mq = m;
+    } else {
+      dq += exp2f(m - Mq) * l;
+    }
+  };
+  {
+    float mv[8], lv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int s2 = quarter + 4 * j;
+      const bool in = row < pm.n_rows && s2 < n;
+      mv[j] = in ? __ldcg(mx + row * S + s2) : -INFINITY;
+      lv[j] = in ? __ldcg(sm + row * S + s2) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      take(mv[j], lv[j]);
+      ms.m[quarter + 4 * j][row] = mv[j];
+    }
+  }
+  if (row < pm.n_rows)
+    for (int s2 = quarter + 4 * 8; s2 < n; s2 += 4) take(__ldcg(mx + row * S + s2), __ldcg(sm + row * S + s2));
+  ms.part_m[quarter][row] = Mq;
+  ms.part_d[quarter][row] = dq;
+  named_bar_sync(kMergeBar, kMergeThreads);
+  if (quarter == 0) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) M = fmaxf(M, ms.part_m[k][row]);
+    float d = 0.0f;
+    if (M != -INFINITY)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (ms.part_m[k][row] != -INFINITY) d += exp2f(ms.part_m[k][row] - M) * ms.part_d[k][row];
+    ms.M[row] = M;
+    ms.inv[row] = d > 0.0f ? 1.0f / d : 0.0f;
+    if (write_lse && row < pm.n_rows) p.lse[pm.row_base + row] = d > 0.0f ? (M + log2f(d)) * kLn2 : -INFINITY;
+  }
+  named_bar_sync(kMergeBar, kMergeThreads);
+}
+
+// One pass of the in-kernel merge (kBlocks = 1 or 2): output dims dim_lo ..
+// dim_lo + 64 * kBlocks - 1 of a unit from its n parts, as the segment merge does [vLLM #51705,
+// 实现拆解 4, merge_mla_segments_triton]: out = sum_s 2^(m_s - M) acc_s / den.
+// Thread t takes dim dim_lo + t % D (D = 64 kBlocks) for the row octets
+// (t / D) * 8 / G .. (one 16-byte load per octet and part from the part's
+// row-octet-major block; a warp's load covers D >= 64 consecutive dims of one
+// octet, whole 128-byte runs).  Every part of a unit holds a token of its
+// longest row, and rows without one in a part hold zeros there, so no
+// liveness pass is needed: a zero weight selects 0.
+template <int kBlocks>
+__device__ void merge_unit_pass(const Params &p, const PendMerge &pm, int dim_lo, int tid, MergeScratch &ms) {
+  constexpr int D = 64 * kBlocks;      // dims of this pass
+  constexpr int G = kMergeThreads / D; // thread groups over the row octets
+  constexpr int OP = 8 / G;            // octets per thread
+  constexpr int BATCH = 16 / OP;       // parts whose loads are in flight at once
+  const int S = p.num_segments, n = pm.n_parts;
+  const int dl = tid % D, grp = tid / D;
+  const int dim = dim_lo + dl;
+  const float *mx = p.segm_max + static_cast<int64_t>(pm.row_base) * S;
+  const int64_t blk0 = (static_cast<int64_t>(pm.b) * p.row_blocks + pm.rb) * S;
+  float a[OP * 8];
+#pragma unroll
+  for (int k = 0; k < OP * 8; ++k) a[k] = 0.0f;
+  for (int c0 = 0; c0 < n; c0 += kMergeSlots) {
+    const int nc = min(kMergeSlots, n - c0);
+    for (int i = tid; i < nc * kRows; i += kMergeThreads) {  // normalised weights of these parts
+      const int sc = i / kRows, rr = i % kRows;
+      float w = 0.0f;
+      if (rr < pm.n_rows && ms.M[rr] != -INFINITY) {
+        const float m = c0 == 0 ? ms.m[sc][rr] : __ldcg(mx + rr * S + c0 + sc);
+        if (m != -INFINITY) w = exp2f(m - ms.M[rr]) * ms.inv[rr];
+      }
+      ms.w[sc][rr] = w;
+    }
+    named_bar_sync(kMergeBar, kMergeThreads);
+    for (int i0 = 0; i0 < nc; i0 += BATCH) {
+      uint4 x[BATCH][OP];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        if (i0 + u < nc) {
+          const uint4 *blk = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + c0 + i0 + u) * (512 * kRows));
+#pragma unroll
+          for (int o = 0; o < OP; ++o) x[u][o] = __ldcg(blk + (grp * OP + o) * 512 + dim);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        if (i0 + u >= nc) break;
+#pragma unroll
+        for (int o = 0; o < OP; ++o) {
+          const int r0 = 8 * (grp * OP + o);
+          const float4 wa = *reinterpret_cast<const float4 *>(&ms.w[i0 + u][r0]);
+          const float4 wb = *reinterpret_cast<const float4 *>(&ms.w[i0 + u][r0 + 4]);
+          const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+          const uint32_t vv[4] = {x[u][o].x, x[u][o].y, x[u][o].z, x[u][o].w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // a weight of 0 selects 0
+            const float e = __uint_as_float((k & 1) ? (vv[k >> 1] & 0xffff0000u) : (vv[k >> 1] << 16));
+            a[8 * o + k] += (w[k] != 0.0f) ? w[k] * e : 0.0f;
+          }
+        }
+      }
+    }
+    named_bar_sync(kMergeBar, kMergeThreads);  // weights are refilled by the next 32 parts
+  }
+  // [row][dim] through shared memory, then the rows' D dims out in 16-byte pieces
+#pragma unroll
+  for (int o = 0; o < OP; ++o)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const __nv_bfloat16 hv = __float2bfloat16_rn(a[8 * o + k]);
+      ms.o[8 * (grp * OP + o) + k][dl] = *reinterpret_cast<const uint16_t *>(&hv);
+    }
+  named_bar_sync(kMergeBar, kMergeThreads);
+  constexpr int kPieces = kRows * D / 8;  // 16-byte pieces of the pass
+  for (int i = tid; i < kPieces; i += kMergeThreads) {
+    const int r = i / (D / 8), c16 = i % (D / 8);
+    if (r < pm.n_rows) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(&ms.o[r][8 * c16]);
+      *reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(pm.row_base) + r) * 512 + dim_lo + 8 * c16) = v;
+    }
+  }
+  named_bar_sync(kMergeBar, kMergeThreads);  // scratch is reused by the next pass
+}
+
+// Merges a staged unit's claimed run of dims from shared memory (statistics
+// already in ms, copies complete): passes of up to 128 dims, thread t taking
+// dim t % Dp of the pass for the row octets (t / Dp) * 8 / G .., weights from
+// ms.w (a zero weight selects 0), then the rows out in 16-byte pieces.
+__device__ void merge_unit_from_stage(const Params &p, const PendMerge &pm, const uint8_t *stage, int tid,
+                                      MergeScratch &ms) {
+  int b0, nb;
+  todo_run(pm.todo, b0, nb);
+  const int D = 64 * nb, n = pm.n_parts;
+  const uint4 *st = reinterpret_cast<const uint4 *>(stage + pm.staged);
+  for (int pass0 = 0; pass0 < D; pass0 += 128) {
+    const int Dp = min(128, D - pass0);  // 128 or 64
+    const int G = kMergeThreads / Dp;    // 2 or 4 row-octet groups
+    const int OP = 8 / G;                // 4 or 2 octets per thread
+    const int dl = tid % Dp, grp = tid / Dp;
+    float a[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) a[k] = 0.0f;
+    for (int u = 0; u < n; ++u) {
+#pragma unroll
+      for (int o = 0; o < 4; ++o) {
+        if (o >= OP) break;
+        const int oc = grp * OP + o;
+        const uint4 xv = st[(u * 8 + oc) * D + pass0 + dl];
+        const float4 wa = *reinterpret_cast<const float4 *>(&ms.w[u][8 * oc]);
+        const float4 wb = *reinterpret_cast<const float4 *>(&ms.w[u][8 * oc + 4]);
+        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        const uint32_t vv[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // a weight of 0 selects 0
+          const float e = __uint_as_float((k & 1) ? (vv[k >> 1] & 0xffff0000u) : (vv[k >> 1] << 16));
+          a[8 * o + k] += (w[k] != 0.0f) ? w[k] * e : 0.0f;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+      if (o >= OP) break;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const __nv_bfloat16 hv = __float2bfloat16_rn(a[8 * o + k]);
+        ms.o[8 * (grp * OP + o) + k][dl] = *reinterpret_cast<const uint16_t *>(&hv);
+      }
+    }
+    named_bar_sync(kMergeBar, kMergeThreads);
+    const int pieces = kRows * Dp / 8;
+    for (int i = tid; i < pieces; i += kMergeThreads) {
+      const int r = i / (Dp / 8), c16 = i % (Dp / 8);
+      if (r < pm.n_rows) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&ms.o[r][8 * c16]);
+        *reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(pm.row_base) + r) * 512 + 64 * b0 + pass0 + 8 * c16) = v;
+      }
+    }
+    named_bar_sync(kMergeBar, kMergeThreads);  // ms.o is reused by the next pass
+  }
+}
+
+// The normalised weights of a unit's first 32 parts into ms.w (statistics in ms).
+__device__ void merge_unit_weights(const PendMerge &pm, int tid, MergeScratch &ms) {
+  const int nc = min(kMergeSlots, pm.n_parts);
+  for (int i = tid; i < nc * kRows; i += kMergeThreads) {
+    const int sc = i / kRows, rr = i % kRows;
+    float w = 0.0f;
+    if (rr < pm.n_rows && ms.M[rr] != -INFINITY) {
+      const float m = ms.m[sc][rr];
+      if (m != -INFINITY) w = exp2f(m - ms.M[rr]) * ms.inv[rr];
+    }
+    ms.w[sc][rr] = w;
+  }
+  named_bar_sync(kMergeBar, kMergeThreads);
+}
+
+// Merges the 64-dim output blocks in pm.todo (bit k: dims 64k .. 64k+63) of
+// one unit: the statistics once, then runs of consecutive blocks in passes
+// of two blocks or one.  The LSE is written by whoever merges block 0.
+__device__ void merge_unit(const Params &p, const PendMerge &pm, int tid, MergeScratch &ms) {
+  merge_unit_stats(p, pm, (pm.todo & 1u) != 0, tid, ms);
+  unsigned todo = pm.todo;
+  while (todo != 0) {
+    const int b0 = __ffs(todo) - 1;
+    int run = 0;
+    while (b0 + run < 8 && ((todo >> (b0 + run)) & 1u)) ++run;
+    const int take = run >= 2 ? 2 : 1;
+    if (take == 2) merge_unit_pass<2>(p, pm, 64 * b0, tid, ms);
+    else merge_unit_pass<1>(p, pm, 64 * b0, tid, ms);
+    todo &= ~(((1u << take) - 1u) << b0);
+  }
+}
+
+template <bool kFp8, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                       const Params p) {
@@ -298,6 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = p.num_segments;
   const int P = p.page_size;
   const bool direct = (S == 1);
+  constexpr bool fused = kFused;  // balanced split merged in this kernel (MLA_DECODE_FUSED_MERGE)
 
   // ---- setup: TMEM, barriers
   if (warp == kMmaWarp) {
@@ -321,9 +653,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&misc.work_empty[i]), 1 + kNumSoftmaxWarps);
     }
     misc.abort = 0;
+    misc.n_pend = 0;
     fence_mbar_init();
   }
   const bool balanced = p.balanced != 0;
+  // Balanced split: the producer's one chunk claim, issued now so that its
+  // round trip overlaps the unit table below.
+  int first_claim = 0;
+  if (balanced && warp == kProducerWarp && lane == 0) first_claim = atomicAdd(p.sched, 1);
   if (balanced) {
     // tiles of every (view, request, row block) unit: the request's longest
     // visible length in 64-token tiles, 0 for a row block without rows
@@ -365,8 +702,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int run = P < kTileTok ? P : kTileTok;
     const int box_bytes = run * (kFp8 ? 64 : 128);
     // A stage is refilled only after its previous tile was consumed, so at
-    // most one load per stage is in flight: remember the latest one.
+    // most one load per stage is in flight: remember the latest one (and the
+    // latest Q load), for the exit path.
     uint32_t armed = 0, armed_par = 0;
+    bool q_armed = false;
+    uint32_t q_par = 0;
     uint32_t g = 0, kq = 0;  // running tile / Q-load counters
     bool ok = true;
     // Longest items first (the tail of the dynamic schedule is set by the
@@ -425,7 +765,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto chunk_of = [&](int x) {
       return static_cast<int>((static_cast<long long>(x + 1) * n_chunks - 1) / T);
     };
+    // Each CTA claims one chunk at most (n_chunks <= grid): a chunk then
+    // holds at most two multi-part units, its first and its last.
     int chunk = -1, c_lo = 0, c_hi = 0, c_hi_ext = 0, u_next = 0;
+    bool claimed = false;
     for (uint32_t k = 0;; ++k) {
       const uint32_t ws = k % kWorkRing;
       WorkEntry &e = misc.work[ws];
@@ -438,12 +781,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next part: (view, request, row block), segment slot, tile range
       bool done = !ok;
       int w = 0, v = 0, b = 0, rb = 0, seg = 0, fill_hi = 0, t_a = 0, t_b = 0, u_start = 0;
+      int unit = 0, n_parts = 0, c_last = 0;
       if (!done && balanced) {
         while (true) {
           if (chunk < 0) {
-            int c = 0;
-            if (lane == 0) c = atomicAdd(p.sched, 1);
-            c = __shfl_sync(0xffffffffu, c, 0);
+            if (claimed) {
+              done = true;
+              break;
+            }
+            claimed = true;
+            const int c = __shfl_sync(0xffffffffu, first_claim, 0);
             if (c >= n_chunks) {
               done = true;
               break;
@@ -472,12 +819,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               t_a = t_b = start;
               seg = 0;
               fill_hi = S;
+              n_parts = 0;
+              c_last = chunk;
             } else {
               t_a = max(c_lo, start);
               t_b = min(c_hi, end);
               seg = chunk - chunk_of(start);
               fill_hi = end <= c_hi ? S : seg + 1;  // its last part marks the slots no chunk reached
+              c_last = chunk_of(end - 1);
+              n_parts = c_last - chunk_of(start) + 1;
             }
+            unit = u;
             u_start = start;
             const int vb = u / p.row_blocks;
             rb = u - vb * p.row_blocks;
@@ -520,6 +872,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         e.w = w;
         e.seg = seg;
         e.fill_hi = fill_hi;
+        e.unit = unit;
+        e.n_parts = n_parts;
+        e.c_last = c_last;
         if (balanced) {
           e.seg_lo = (t_a - u_start) * kTileTok;
           e.seg_hi = min((t_b - u_start) * kTileTok, group_len);
@@ -561,6 +916,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane < kNumChunks)
             tma_load_2d(s_q + lane * kQChunkBytes, &tm_q, q_bar, lane * 64, q_row, pol_q);
+          q_armed = true;
+          q_par = kq & 1u;
         }
         ++kq;
         for (int i = 0; i < n_tiles && ok; ++i, ++g) {
@@ -626,10 +983,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     if (lane == 0 && (!ok || *abort_flag)) {
-      // Let the copies already issued land before the CTA's memory is released.
+      // Let the copies already issued land before the CTA's memory is
+      // released (a copy completes by itself; this wait has its own budget).
       const volatile int never = 0;
       for (int st = 0; st < kStages; ++st)
-        if (armed & (1u << st)) mbar_wait(smem_u32(&misc.full[st]), (armed_par >> st) & 1u, &never, budget);
+        if (armed & (1u << st))
+          mbar_wait(smem_u32(&misc.full[st]), (armed_par >> st) & 1u, &never, p.drain_budget);
+      if (q_armed) mbar_wait(smem_u32(&misc.q_full), q_par, &never, p.drain_budget);
     }
   } else if (warp == kMmaWarp) {
     // ======================================================== UMMA issuer
@@ -751,9 +1111,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      umma_commit(smem_u32(&misc.fin));
+      umma_commit(smem_u32(&misc.fin));  // every MMA issued so far has retired
       const volatile int never = 0;
-      mbar_wait(smem_u32(&misc.fin), 0, &never, budget);
+      mbar_wait(smem_u32(&misc.fin), 0, &never, p.drain_budget);
     }
   } else {
     // ======================================================== softmax warps
@@ -785,11 +1145,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const WorkEntry &e = misc.work[ws];
       const int n_rows = e.n_rows, n_tiles = e.n_tiles, seg = e.seg, e_b = e.b, e_rb = e.rb, fill_hi = e.fill_hi;
       const int row_base = e.row_base, seg_lo = e.seg_lo, seg_hi = e.seg_hi;
+      const int n_parts = e.n_parts, c_last = e.c_last, e_unit = e.unit;
+      // normalised bf16 rows + LSE straight from TMEM: one segment, or (in-kernel
+      // merge) a unit whose tiles all lie in this CTA's chunk
+      const bool to_out = direct || (fused && n_parts == 1);
       if (n_rows > 0 && n_tiles == 0) {
         // nothing visible in this segment for any row of the block
         if (wq == 0 && my_col < n_rows) {
           const int64_t r = row_base + my_col;
-          if (direct) {
+          if (direct || fused) {
             p.lse[r] = -INFINITY;
           } else {
             for (int s2 = seg; s2 < max(fill_hi, seg + 1); ++s2) {
@@ -798,7 +1162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (direct && my_col < n_rows) {
+        if ((direct || fused) && my_col < n_rows) {
           uint4 *dst = reinterpret_cast<uint4 *>(p.out + (row_base + my_col) * 512);
           for (int ee = wq; ee < 64; ee += 4) dst[ee] = make_uint4(0, 0, 0, 0);
         }
@@ -973,7 +1337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       red_buf ^= 1;
       if (ok && wq == 0 && my_col < n_rows) {
         const int64_t r = row_base + my_col;
-        if (direct) {
+        if (to_out) {
           p.lse[r] = (l_tot > 0.0f) ? (m_ref + __log2f(l_tot)) * kLn2 : -INFINITY;
         } else {
           p.segm_max[r * S + seg] = (l_tot > 0.0f) ? m_ref : -INFINITY;
@@ -984,7 +1348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const float col_scale = (l_tot > 0.0f) ? (direct ? p.out_scale / l_tot : p.out_scale) : 0.0f;
+      const float col_scale = (l_tot > 0.0f) ? (to_out ? p.out_scale / l_tot : p.out_scale) : 0.0f;
       const int n_cols = min(32, n_rows - 32 * g_col);
       // column j's scale (0: the row saw no token here) gathered once for all four blocks
       float sc[32];
@@ -1009,7 +1373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t (&ov)[32] = ovp[h2];
           if (!ok || *abort_flag != 0) continue;
           const int dim = blk * 128 + dim_lane;
-          if (direct) {
+          if (to_out) {
             __nv_bfloat16 *o = p.out + r0 * 512 + dim;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -1040,6 +1404,116 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();  // O reads done before the next item's first PV overwrites O
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&misc.work_empty[ws]));
+      if (fused && n_parts > 1 && threadIdx.x == 0) {
+        // a part of a multi-part unit: published (and the unit merged) once
+        // this CTA's own work is done
+        if (misc.n_pend < kMaxPend) {
+          PendMerge &pm = misc.pend[misc.n_pend++];
+          pm.b = e_b;
+          pm.rb = e_rb;
+          pm.row_base = row_base;
+          pm.n_rows = n_rows;
+          pm.n_parts = n_parts;
+          pm.unit = e_unit;
+          pm.seg = seg;
+          pm.c_last = c_last;
+        } else {
+          record_error(p.err, MLA_DEV_WAIT_TIMEOUT);  // cannot happen: one chunk per CTA
+        }
+      }
+    }
+    if (fused) {
+      // The CTA's own parts are done: every tile's PV has retired and no copy
+      // is in flight, so stage 0 is free for the merge scratch.  Publish the
+      // parts: every thread's stores are fenced before the barrier, then one
+      // release add per part counts it.  A holder that will wait for its
+      // unit -- only when every chunk of the unit is claimed, i.e. held by a
+      // running CTA, which publishes without waiting on anyone -- claims its
+      // share of the eight 64-dim output blocks in the same add; the holder
+      // of the last part to arrive merges every block nobody claimed.
+      __threadfence();
+      named_bar_sync(kMergeBar, kMergeThreads);
+      const int n_pend = misc.n_pend;
+      if (threadIdx.x == 0) {
+        for (int i = 0; i < n_pend; ++i) {
+          PendMerge &pm = misc.pend[i];
+          // holder k of n takes the consecutive blocks [8k / n, 8(k+1) / n)
+          const int blo = (8 * pm.seg) / pm.n_parts, bhi = (8 * (pm.seg + 1)) / pm.n_parts;
+          const unsigned mine = ((1u << bhi) - 1u) & ~((1u << blo) - 1u);
+          const bool can_wait = ld_volatile(p.sched) > pm.c_last;
+          const unsigned add = 1u + (can_wait ? (mine << 16) : 0u);
+          const unsigned old = atom_add_release_gpu(p.unit_state + pm.unit, add);
+          const bool last = (old & 0xffffu) == static_cast<unsigned>(pm.n_parts - 1);
+          pm.todo = last ? (~(old >> 16) & 0xffu) : (can_wait ? mine : 0u);
+          pm.wait = last ? 0 : 1;
+        }
+      }
+      // staging plan: a unit whose claim is one run of blocks and whose parts'
+      // slices fit the remaining staging area is copied into shared memory
+      // (all copies in flight at once); others are read from L2 directly
+      if (threadIdx.x == 0) {
+        int used = 0;
+        for (int i = 0; i < n_pend; ++i) {
+          PendMerge &pm = misc.pend[i];
+          pm.staged = -1;
+          if (pm.todo == 0 || pm.n_parts > kMergeSlots) continue;
+          int b0, nb;
+          todo_run(pm.todo, b0, nb);
+          const int bytes = pm.n_parts * 8 * 64 * nb * 16;
+          if (nb > 0 && used + bytes <= kStagingBytes) {
+            pm.staged = used;
+            used += bytes;
+          }
+        }
+      }
+      named_bar_sync(kMergeBar, kMergeThreads);
+      fence_proxy_async_smem();
+      MergeScratch &ms = *reinterpret_cast<MergeScratch *>(smem + kOffQ);
+      const uint8_t *stage_gen = smem + kOffStages;
+      // Two-step pipeline over the pending units: wait (bounded) for unit i
+      // and issue its copies, then merge unit i - 1 while they fly.
+      auto merge_pending = [&](int i, int later) {
+        const PendMerge pm = misc.pend[i];
+        if (pm.todo == 0 || !pm.go) return;
+        __threadfence();
+        if (pm.staged < 0) {
+          merge_unit(p, pm, threadIdx.x, ms);
+          return;
+        }
+        merge_unit_stats(p, pm, (pm.todo & 1u) != 0, threadIdx.x, ms);
+        merge_unit_weights(pm, threadIdx.x, ms);
+        if (later > 0) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        named_bar_sync(kMergeBar, kMergeThreads);
+        merge_unit_from_stage(p, pm, stage_gen, threadIdx.x, ms);
+      };
+      for (int i = 0; i < n_pend; ++i) {
+        if (threadIdx.x == 0) {
+          PendMerge &pm = misc.pend[i];
+          bool go = pm.todo != 0 && ok && *abort_flag == 0;
+          if (go && pm.wait) {  // bounded wait for the unit's other parts
+            const long long t0 = clock64();
+            while ((ld_acquire_gpu(p.unit_state + pm.unit) & 0xffffu) != static_cast<unsigned>(pm.n_parts)) {
+              if (*abort_flag || clock64() - t0 > budget) {
+                fail();
+                go = false;
+                break;
+              }
+              __nanosleep(64);
+            }
+          }
+          pm.go = go ? 1 : 0;
+        }
+        __syncwarp();
+        named_bar_sync(kMergeBar, kMergeThreads);
+        if (misc.pend[i].go && misc.pend[i].staged >= 0) {
+          __threadfence();
+          stage_unit(p, misc.pend[i], s_stage0, threadIdx.x);
+        }
+        cp_async_commit();  // one group per pending unit (empty when not staged)
+        if (i > 0) merge_pending(i - 1, 1);
+      }
+      if (n_pend > 0) merge_pending(n_pend - 1, 0);
     }
   }
 
@@ -1051,12 +1525,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-bool g_attr_set[2][64];
-int g_num_sms[64];
+// Per-device caches filled on first use (relaxed atomics: concurrent first
+// calls store the same values).
+std::atomic<bool> g_attr_set[4][64];  // [fp8 + 2 * fused][device]
+std::atomic<int> g_num_sms[64];
 
 }  // namespace
 
-mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
+mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream, bool *merged) {
+  *merged = false;
   const mla_decode_args &a = *d.a;
   const bool fp8 = a.kv_dtype == MLA_KV_FP8_E4M3;
   CUtensorMap tm_q, tm_kv;
@@ -1085,17 +1562,21 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
     set_error("device ordinal %d out of range", dev);
     return MLA_ERR_CUDA;
   }
-  auto kern = fp8 ? mla_decode_kernel<true> : mla_decode_kernel<false>;
-  if (!g_attr_set[fp8][dev]) {
+  // the in-kernel merge is its own instantiation: the default kernel holds none of its code
+  const bool fuse_req = (a.flags & MLA_DECODE_FUSED_MERGE) != 0;
+  auto kern = fp8 ? (fuse_req ? mla_decode_kernel<true, true> : mla_decode_kernel<true, false>)
+                  : (fuse_req ? mla_decode_kernel<false, true> : mla_decode_kernel<false, false>);
+  const int kind = (fp8 ? 1 : 0) + (fuse_req ? 2 : 0);
+  if (!g_attr_set[kind][dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode smem)");
-    g_attr_set[fp8][dev] = true;
+    g_attr_set[kind][dev].store(true, std::memory_order_relaxed);
   }
-  if (g_num_sms[dev] == 0) {
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  int num_sms = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (num_sms == 0) {
+    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
-    g_num_sms[dev] = n;
+    g_num_sms[dev].store(num_sms, std::memory_order_relaxed);
   }
 
   Params p{};
@@ -1110,7 +1591,9 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
   p.err = d.err;
   p.sched = d.sched;
   p.num_cache_rows = a.num_cache_rows;
-  p.wait_budget = 4000000000LL;  // ~2 s of SM clock
+  constexpr long long kDefaultBudget = 4000000000LL;  // ~2 s of SM clock
+  p.wait_budget = a.wait_cycles > 0 ? static_cast<long long>(a.wait_cycles) : kDefaultBudget;
+  p.drain_budget = kDefaultBudget;
   p.subpage_stride = a.subpage_stride;
   p.page_size = a.page_size;
   p.num_heads = a.num_heads;
@@ -1137,13 +1620,21 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream) {
                 units * max_unit_tiles <= INT32_MAX)
                    ? 1
                    : 0;
+  p.unit_state = d.unit_state;
+  p.fused = fuse_req ? 1 : 0;
+  if (fuse_req && !p.balanced) {
+    set_error("mla_decode_verify: MLA_DECODE_FUSED_MERGE needs the balanced split (num_segments > 1, "
+              "at most %d units, no MLA_DECODE_UNIFORM_SEGMENTS)", kMaxUnits);
+    return MLA_ERR_UNSUPPORTED;
+  }
+  *merged = fuse_req;
   const float kv_scale = fp8 ? a.kv_scale : 1.0f;
   p.score_scale_log2 = static_cast<float>(static_cast<double>(a.sm_scale) * kv_scale * 1.4426950408889634);
   p.out_scale = kv_scale;
 
-  const int grid = static_cast<int>(items < g_num_sms[dev] ? items : g_num_sms[dev]);
-  e = cudaMemsetAsync(d.sched, 0, sizeof(int), stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(work counter)");
+  const int grid = static_cast<int>(items < num_sms ? items : num_sms);
+  e = cudaMemsetAsync(d.sched, 0, d.state_bytes, stream);  // work counter + unit counters
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(work counters)");
   kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");

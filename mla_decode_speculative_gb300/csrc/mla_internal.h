@@ -39,8 +39,10 @@ struct TableLaunch {  // optional sub-page expansion (block_table == nullptr: no
 mla_status launch_plan_rows(int num_reqs, int num_rows, const int32_t *seq_lens,
                             const int32_t *qo_indptr, int32_t *row_len, int32_t *row_req,
                             const TableLaunch &table, int *err, cudaStream_t stream);
+// Views rank .. rank + num_views - 1 (blockIdx.y), outputs and tables at
+// per-view strides T, B * sp_stride and B * bt_stride.
 mla_status launch_shard_rows(int num_reqs, int num_rows, const int32_t *qo_indptr,
-                             const int32_t *row_len_global, int world_size, int rank,
+                             const int32_t *row_len_global, int world_size, int rank, int num_views,
                              int interleave, int32_t *row_len_local, const TableLaunch &table,
                              int *err, cudaStream_t stream);
 
@@ -49,16 +51,23 @@ struct DecodeLaunch {
   uint16_t *segm_out;  // bf16
   float *segm_max;
   float *segm_sum;
-  int *sched;  // work-claim counter (workspace), zeroed before each launch
+  int *sched;           // work-claim counter (workspace), zeroed before each launch
+  unsigned *unit_state; // per-unit part counters (workspace, after sched), zeroed with it
+  size_t state_bytes;   // bytes from sched through the unit counters
   int *err;
 };
 // Workspace layout of mla_decode_verify: [segm_out][segm_max][segm_sum] (only
-// when num_segments > 1, 256-byte aligned regions) then the work counter.
+// when num_segments > 1, 256-byte aligned regions), then 256 bytes of work
+// counter, then (num_segments > 1) one 32-bit counter per (view, request,
+// 64-row block) unit.
 struct WorkspaceLayout {
-  size_t segm_out, segm_max, segm_sum, sched, total;
+  size_t segm_out, segm_max, segm_sum, sched, unit_state, total;
 };
 WorkspaceLayout decode_workspace_layout(const mla_decode_args &a);
-mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream);
+// Launches the decode.  *merged is set when the kernel also merged the
+// split-K parts into out / lse itself (balanced split), so no merge launch
+// must follow.
+mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream, bool *merged);
 
 struct MergeLaunch {
   int mode;

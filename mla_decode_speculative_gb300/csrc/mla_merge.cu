@@ -82,19 +82,24 @@ __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x 
 
 // ---------------------------------------------------------------- segments
 constexpr int kSegChunk = 32;  // segments whose weights are staged at a time
+constexpr int kSegBatch = 8;   // live segments whose partial blocks are read at a time
 
-// grid (B * RB, 512 / 64), 256 threads.  The block's 64 rows x S statistics
-// are contiguous; one pass gives every row its max and denominator (a
-// running pair per thread, rescaled as the max grows), then the normalised
-// weights 2^(m_s - M) / den of 32 segments at a time go to shared memory, the
-// segments with a non-zero weight are listed, and their partial blocks are
-// read eight at a time.
-__global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
+// grid (V * B * RB, 512 / 64), 256 threads: one (view, request, row block)
+// unit x 64 output dims.  The unit's 64 rows x S statistics are contiguous:
+// one pass gives every row its max and denominator (four threads per row,
+// each a running pair rescaled as its max grows) and keeps the maxima of the
+// first 32 segments in shared memory; the normalised weights 2^(m_s - M) / den
+// of 32 segments at a time are then formed there, the segments with a
+// non-zero weight listed, and their partial blocks read eight at a time.
+// Warp w takes dims 8w .. 8w+7 of the CTA's 64, lane l dim 8w + l % 8 for the
+// row octets l / 8 and l / 8 + 4: every load instruction of a warp covers
+// four whole 128-byte runs (eight consecutive dims of one octet).
+__global__ void __launch_bounds__(256, 2) merge_segment_blocks(const SegParams p) {
+  __shared__ __align__(16) float s_m[kSegChunk][kBlockRows];
   __shared__ __align__(16) float s_w[kSegChunk][kBlockRows];
-  __shared__ __align__(16) uint32_t s_o[kBlockRows][kDimsPerCta / 2 + 4];  // bf16 pairs, padded rows
-  __shared__ int s_live[kSegChunk];
+  __shared__ __align__(16) uint16_t s_o[kBlockRows][kDimsPerCta + 8];  // bf16 [row][dim], padded rows
   __shared__ float s_part[4][kBlockRows], s_dpart[4][kBlockRows];
-  __shared__ int s_list[kSegChunk], s_nlive;
+  __shared__ int s_live[kSegChunk], s_list[kSegChunk], s_nlive;
   __shared__ float s_M[kBlockRows], s_inv[kBlockRows];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // block (view, request, row block): vb = v * B + b
@@ -110,22 +115,34 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
   const float *mx = p.segm_max + grow0 * S;  // [64 rows][S], contiguous
   const float *sm = p.segm_sum + grow0 * S;
 
-  // per-row max and denominator in one pass: four threads per row, segments
-  // strided by 4, each keeping a running (max, sum) rescaled as the max grows
   const int row = tid & (kBlockRows - 1), quarter = tid >> 6;
   float Mq = -INFINITY, dq = 0.0f;
-  if (row < n_rows)
-    for (int s = quarter; s < S; s += 4) {
-      const float m = mx[row * S + s];
-      if (m == -INFINITY) continue;
-      const float l = sm[row * S + s];
-      if (m > Mq) {
-        dq = dq * exp2f(Mq - m) + l;  // 0 while Mq is -inf
-        Mq = m;
-      } else {
-        dq += exp2f(m - Mq) * l;
-      }
+  auto take = [&](float m, float l) {
+    if (m == -INFINITY) return;
+    if (m > Mq) {
+      dq = dq * exp2f(Mq - m) + l;  // 0 while Mq is -inf
+      Mq = m;
+    } else {
+      dq += exp2f(m - Mq) * l;
     }
+  };
+  {
+    float mv[8], lv[8];  // the first 32 segments, loaded at once
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int s2 = quarter + 4 * j;
+      const bool in = row < n_rows && s2 < S;
+      mv[j] = in ? mx[row * S + s2] : -INFINITY;
+      lv[j] = in ? sm[row * S + s2] : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      take(mv[j], lv[j]);
+      s_m[quarter + 4 * j][row] = mv[j];
+    }
+  }
+  if (row < n_rows)
+    for (int s2 = quarter + 4 * 8; s2 < S; s2 += 4) take(mx[row * S + s2], sm[row * S + s2]);
   s_part[quarter][row] = Mq;
   s_dpart[quarter][row] = dq;
   __syncthreads();
@@ -145,12 +162,11 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
   }
   __syncthreads();
 
-  const int dim0 = blockIdx.y * kDimsPerCta + warp * 8;
-  const int oct = lane >> 2;          // rows 8 oct .. 8 oct + 7 of the block
-  const int dp = 2 * (lane & 3);      // dims dim0 + dp, dim0 + dp + 1
-  float a0[8], a1[8];                 // [row of the octet] for the two dims
+  const int dim = blockIdx.y * kDimsPerCta + warp * 8 + (lane & 7);
+  const int og = lane >> 3;  // row octets og and og + 4
+  float a[16];               // rows 8 og + k (k < 8) and 8 (og + 4) + k - 8
 #pragma unroll
-  for (int k = 0; k < 8; ++k) a0[k] = a1[k] = 0.0f;
+  for (int k = 0; k < 16; ++k) a[k] = 0.0f;
   const int64_t blk0 = (static_cast<int64_t>(vb) * p.row_blocks + rb) * S;
   for (int c0 = 0; c0 < S; c0 += kSegChunk) {
     const int nc = min(kSegChunk, S - c0);
@@ -161,7 +177,7 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
       const int sc = i / kBlockRows, rr = i % kBlockRows;
       float w = 0.0f;
       if (rr < n_rows && s_M[rr] != -INFINITY) {
-        const float m = mx[rr * S + c0 + sc];
+        const float m = c0 == 0 ? s_m[sc][rr] : mx[rr * S + c0 + sc];
         if (m != -INFINITY) w = exp2f(m - s_M[rr]) * s_inv[rr];
       }
       s_w[sc][rr] = w;
@@ -176,104 +192,132 @@ __global__ void __launch_bounds__(256) merge_segment_blocks(const SegParams p) {
     }
     __syncthreads();
     const int n_live = s_nlive;
-    for (int i0 = 0; i0 < n_live; i0 += 8) {
-      uint4 x[8][2];
+    for (int i0 = 0; i0 < n_live; i0 += kSegBatch) {
+      uint4 x[kSegBatch][2];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kSegBatch; ++u) {
         if (i0 + u < n_live) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + c0 + s_list[i0 + u]) * (512 * kBlockRows)) +
-                             oct * 512 + dim0 + dp;
-          x[u][0] = __ldcs(src);
-          x[u][1] = __ldcs(src + 1);
-        } else {
-          x[u][0] = x[u][1] = make_uint4(0u, 0u, 0u, 0u);
+          const uint4 *blk = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + c0 + s_list[i0 + u]) * (512 * kBlockRows));
+          x[u][0] = __ldcs(blk + og * 512 + dim);
+          x[u][1] = __ldcs(blk + (og + 4) * 512 + dim);
         }
       }
       // a weight of 0 selects 0: an empty row's slot is never used as a value
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kSegBatch; ++u) {
         if (i0 + u >= n_live) break;
         const int sc = s_list[i0 + u];
-        const float4 wa = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oct]);
-        const float4 wb = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oct + 4]);
-        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-        const uint32_t v0[4] = {x[u][0].x, x[u][0].y, x[u][0].z, x[u][0].w};
-        const uint32_t v1[4] = {x[u][1].x, x[u][1].y, x[u][1].z, x[u][1].w};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float e0 = (k & 1) ? bf16_hi(v0[k >> 1]) : bf16_lo(v0[k >> 1]);
-          const float e1 = (k & 1) ? bf16_hi(v1[k >> 1]) : bf16_lo(v1[k >> 1]);
-          a0[k] += (w[k] != 0.0f) ? w[k] * e0 : 0.0f;
-          a1[k] += (w[k] != 0.0f) ? w[k] * e1 : 0.0f;
+        for (int h = 0; h < 2; ++h) {
+          const float4 wa = *reinterpret_cast<const float4 *>(&s_w[sc][8 * (og + 4 * h)]);
+          const float4 wb = *reinterpret_cast<const float4 *>(&s_w[sc][8 * (og + 4 * h) + 4]);
+          const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+          const uint32_t vv[4] = {x[u][h].x, x[u][h].y, x[u][h].z, x[u][h].w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float e = (k & 1) ? bf16_hi(vv[k >> 1]) : bf16_lo(vv[k >> 1]);
+            a[8 * h + k] += (w[k] != 0.0f) ? w[k] * e : 0.0f;
+          }
         }
       }
     }
     __syncthreads();  // s_w / s_live are refilled by the next chunk
   }
-  // transpose through shared memory: row 8 oct + k, dims (warp * 8 + dp, +1)
+  // transpose through shared memory: this thread's dim for rows 8 og + k and 8 (og + 4) + k
 #pragma unroll
-  for (int k = 0; k < 8; ++k) s_o[8 * oct + k][warp * 4 + (lane & 3)] = pack_bf16(a0[k], a1[k]);
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const __nv_bfloat16 hv = __float2bfloat16_rn(a[8 * h + k]);
+      s_o[8 * (og + 4 * h) + k][warp * 8 + (lane & 7)] = *reinterpret_cast<const uint16_t *>(&hv);
+    }
   __syncthreads();
   // 64 rows x 128 bytes: thread t writes 16-byte pieces t and t + 256
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int i = tid + 256 * h, r = i >> 3, c16 = i & 7;
     if (r < n_rows) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(&s_o[r][4 * c16]);
-      *reinterpret_cast<uint4 *>(p.out + (grow0 + r) * 512 + blockIdx.y * kDimsPerCta + 8 * c16) = v;
+      const uint4 val = *reinterpret_cast<const uint4 *>(&s_o[r][8 * c16]);
+      *reinterpret_cast<uint4 *>(p.out + (grow0 + r) * 512 + blockIdx.y * kDimsPerCta + 8 * c16) = val;
     }
   }
 }
 
 // ---------------------------------------------------------------- states
+constexpr int kStateWarps = 4;  // (row, head) items per 128-thread CTA, one per warp
+constexpr int kStateBatch = 8;  // parts read at a time
+
+// Up to 32 parts: one warp per (row, head).  Lane s holds part s's LSE; lane
+// l covers dims 16 l .. 16 l + 15 of every part (two 16-byte loads per part,
+// a warp's load covering the part's 1 KiB row whole).  The first eight parts'
+// rows are read together with the LSEs (one round trip for up to eight
+// shards); a part with lse = -inf gets weight 0, which selects 0, so its row
+// is never used as a value.
+__global__ void __launch_bounds__(kStateWarps * 32) merge_states_small(const StateParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t it = static_cast<int64_t>(blockIdx.x) * kStateWarps + (threadIdx.x >> 5);
+  if (it >= p.num_items) return;
+  const int n = p.num_parts;
+  auto row_of = [&](int s) {
+    return reinterpret_cast<const uint4 *>(p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512) + 2 * lane;
+  };
+  uint4 x[kStateBatch][2];
+#pragma unroll
+  for (int u = 0; u < kStateBatch; ++u) {
+    if (u < n) {
+      x[u][0] = __ldcs(row_of(u));
+      x[u][1] = __ldcs(row_of(u) + 1);
+    }
+  }
+  const float m = lane < n ? p.part_lse[static_cast<int64_t>(lane) * p.num_items + it] : -INFINITY;
+  const float M = warp_max(m);
+  uint4 *dst = reinterpret_cast<uint4 *>(p.out + it * 512) + 2 * lane;
+  if (M == -INFINITY) {
+    dst[0] = dst[1] = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) p.lse[it] = -INFINITY;
+    return;
+  }
+  const float w = (m != -INFINITY) ? expf(m - M) : 0.0f;
+  const float den = warp_sum(w);
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+  for (int s0 = 0; s0 < n; s0 += kStateBatch) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int u = 0; u < kStateBatch; ++u) {
+        if (s0 + u < n) {
+          x[u][0] = __ldcs(row_of(s0 + u));
+          x[u][1] = __ldcs(row_of(s0 + u) + 1);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kStateBatch; ++u) {
+      const float ws = __shfl_sync(0xffffffffu, w, (s0 + u) & 31);
+      if (s0 + u >= n || ws == 0.0f) continue;
+      const uint32_t vv[8] = {x[u][0].x, x[u][0].y, x[u][0].z, x[u][0].w,
+                              x[u][1].x, x[u][1].y, x[u][1].z, x[u][1].w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc[2 * k] = fmaf(ws, bf16_lo(vv[k]), acc[2 * k]);
+        acc[2 * k + 1] = fmaf(ws, bf16_hi(vv[k]), acc[2 * k + 1]);
+      }
+    }
+  }
+  const float inv_den = 1.0f / den;
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) o[k] = pack_bf16(acc[2 * k] * inv_den, acc[2 * k + 1] * inv_den);
+  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  if (lane == 0) p.lse[it] = M + logf(den);
+}
+
 __device__ __forceinline__ float4 load_state4(const StateParams &p, int64_t it, int s, int tid) {
   const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(
                              p.part_out + (static_cast<int64_t>(s) * p.num_items + it) * 512) + tid);
   return make_float4(bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y));
-}
-
-// Up to 32 parts: no block barrier.  Every thread reads the item's (tiny,
-// L1-broadcast) LSEs itself, so the loads of all live parts are issued
-// together, one dependent round trip after the LSEs.
-__global__ void __launch_bounds__(kThreadsPerItem) merge_states_small(const StateParams p) {
-  const int tid = threadIdx.x;
-  const int64_t it = blockIdx.x;
-  const int n = p.num_parts;
-  float m[32];
-#pragma unroll
-  for (int s = 0; s < 32; ++s) m[s] = (s < n) ? p.part_lse[static_cast<int64_t>(s) * p.num_items + it] : -INFINITY;
-  float M = -INFINITY;
-#pragma unroll
-  for (int s = 0; s < 32; ++s) M = fmaxf(M, m[s]);
-  uint2 *dst = reinterpret_cast<uint2 *>(p.out + it * 512) + tid;
-  if (M == -INFINITY) {
-    *dst = make_uint2(0, 0);
-    if (tid == 0) p.lse[it] = -INFINITY;
-    return;
-  }
-  float den = 0.0f;
-#pragma unroll
-  for (int s = 0; s < 32; ++s) {
-    const float w = (m[s] != -INFINITY) ? expf(m[s] - M) : 0.0f;
-    den += w;
-    m[s] = w;  // m now holds the weights
-  }
-  float4 v[32];
-#pragma unroll
-  for (int s = 0; s < 32; ++s)
-    v[s] = (m[s] != 0.0f) ? load_state4(p, it, s, tid) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-  for (int s = 0; s < 32; ++s) {
-    acc[0] = fmaf(m[s], v[s].x, acc[0]);
-    acc[1] = fmaf(m[s], v[s].y, acc[1]);
-    acc[2] = fmaf(m[s], v[s].z, acc[2]);
-    acc[3] = fmaf(m[s], v[s].w, acc[3]);
-  }
-  const float inv_den = 1.0f / den;
-  *dst = make_uint2(pack_bf16(acc[0] * inv_den, acc[1] * inv_den),
-                    pack_bf16(acc[2] * inv_den, acc[3] * inv_den));
-  if (tid == 0) p.lse[it] = M + logf(den);
 }
 
 // Any number of parts: live parts are compacted, in order, into shared
@@ -395,8 +439,12 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
       return MLA_ERR_UNSUPPORTED;
     }
     const unsigned blocks = static_cast<unsigned>(p.num_items);
-    if (p.num_parts <= 32) merge_states_small<<<blocks, kThreadsPerItem, 0, stream>>>(p);
-    else merge_states<<<blocks, kThreadsPerItem, 0, stream>>>(p);
+    if (p.num_parts <= 32) {
+      const unsigned ctas = static_cast<unsigned>((p.num_items + kStateWarps - 1) / kStateWarps);
+      merge_states_small<<<ctas, kStateWarps * 32, 0, stream>>>(p);
+    } else {
+      merge_states<<<blocks, kThreadsPerItem, 0, stream>>>(p);
+    }
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");

@@ -3,15 +3,15 @@
 //
 // mla_decode_verify needs a scratch workspace (split-K partials and a work
 // counter) that the caller allocates.  Some callers cannot do that at the
-// point of the call: code running inside a CUDA-graph capture, where
-// cudaMalloc is not allowed; serving runtimes that reserve all device memory
-// at start-up and forbid allocation on the request path; plugin hosts and
-// plain C callers that hold no device allocator and for which a cudaMalloc
-// would synchronise the device in the middle of a step.  This file gives them
-// one more entry point whose scratch is a fixed-size array in the library's
-// own device memory.
+// point of the call: serving runtimes that reserve all device memory at
+// start-up and forbid allocation on the request path; plugin hosts and plain
+// C callers that hold no device allocator and for which a cudaMalloc would
+// synchronise the device in the middle of a step.  This file gives them one
+// more entry point whose scratch is a fixed-size array in the library's own
+// device memory.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "mla_gb300.h"
@@ -24,7 +24,9 @@ namespace {
 constexpr size_t kStaticScratchBytes = static_cast<size_t>(MLA_STATIC_SCRATCH_BYTES);
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-void *g_static_scratch_ptr[64];  // device address of the array, per device
+// Device address of the array, per device (relaxed atomic: two threads making
+// their first call at once store the same value).
+std::atomic<void *> g_static_scratch_ptr[64];
 
 // The array's name is a host-side stand-in in host code: its device address
 // is looked up once per device, with that device current.
@@ -36,13 +38,13 @@ mla_status static_scratch(void **out) {
     set_error("device ordinal %d out of range", dev);
     return MLA_ERR_CUDA;
   }
-  if (g_static_scratch_ptr[dev] == nullptr) {
-    void *ptr = nullptr;
+  void *ptr = g_static_scratch_ptr[dev].load(std::memory_order_relaxed);
+  if (ptr == nullptr) {
     e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    g_static_scratch_ptr[dev] = ptr;
+    g_static_scratch_ptr[dev].store(ptr, std::memory_order_relaxed);
   }
-  *out = g_static_scratch_ptr[dev];
+  *out = ptr;
   return MLA_OK;
 }
 

@@ -34,6 +34,7 @@ MLA_MERGE_SEGMENTS = 0
 MLA_MERGE_STATES = 1
 MLA_DECODE_SKIP_MERGE = 1
 MLA_DECODE_UNIFORM_SEGMENTS = 2
+MLA_DECODE_FUSED_MERGE = 4
 
 DEVICE_ERRORS = {0: "MLA_DEV_OK", 1: "MLA_DEV_BAD_INDPTR", 2: "MLA_DEV_BAD_QLEN",
                  3: "MLA_DEV_BAD_BLOCK_ID", 4: "MLA_DEV_LEN_BOUND", 5: "MLA_DEV_BAD_SUBPAGE",
@@ -56,7 +57,7 @@ class DecodeArgs(ctypes.Structure):
                 ("subpage_table", ctypes.c_void_p), ("subpage_stride", ctypes.c_int),
                 ("page_size", ctypes.c_int), ("num_segments", ctypes.c_int),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("flags", ctypes.c_int),
-                ("num_views", ctypes.c_int)]
+                ("num_views", ctypes.c_int), ("wait_cycles", ctypes.c_int64)]
 
 
 class MergeArgs(ctypes.Structure):
@@ -70,7 +71,8 @@ class MergeArgs(ctypes.Structure):
 
 _lib = None
 _lock = threading.Lock()
-EXPORTS = ("mla_page_size", "mla_plan_rows", "mla_shard_row_view", "mla_decode_verify_workspace",
+EXPORTS = ("mla_page_size", "mla_plan_rows", "mla_shard_row_view", "mla_shard_row_views",
+           "mla_decode_verify_workspace",
            "mla_decode_verify", "mla_decode_verify_noalloc", "mla_write_kv", "mla_merge_segments", "mla_get_device_error",
            "mla_last_error_string", "mla_status_string", "mla_abi_version")
 
@@ -99,6 +101,9 @@ def lib():
         L.mla_shard_row_view.argtypes = [c_int, c_int, i32p, i32p, c_int, c_int, c_int, i32p, i32p,
                                          c_int, c_int, c_int, i32p, c_int, vp]
         L.mla_shard_row_view.restype = c_int
+        L.mla_shard_row_views.argtypes = [c_int, c_int, i32p, i32p, c_int, c_int, i32p, i32p, c_int,
+                                          c_int, c_int, i32p, c_int, vp]
+        L.mla_shard_row_views.restype = c_int
         L.mla_decode_verify_workspace.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.mla_decode_verify_workspace.restype = ctypes.c_size_t
         L.mla_decode_verify.argtypes = [ctypes.POINTER(DecodeArgs), vp, ctypes.c_size_t, vp]
@@ -201,9 +206,36 @@ def shard_row_view(qo_indptr: torch.Tensor, row_len_global: torch.Tensor, world_
     return row_len_local, subpage_table
 
 
+def shard_row_views(qo_indptr: torch.Tensor, row_len_global: torch.Tensor, world_size: int,
+                    interleave: int = 1, block_tables: Optional[torch.Tensor] = None,
+                    num_blocks: int = 0, block_size: int = 0, subpage_stride: int = 0,
+                    row_len_local=None, subpage_tables=None, stream=None):
+    """mla_shard_row_views: all W views in one launch.  block_tables [W, B, width];
+    returns (row_len_local [W, T], subpage_tables [W, B, stride] or None)."""
+    B = int(qo_indptr.shape[0]) - 1
+    T = int(row_len_global.shape[0])
+    W = int(world_size)
+    dev = row_len_global.device
+    if row_len_local is None:
+        row_len_local = torch.empty((W, T), dtype=torch.int32, device=dev)
+    bt_stride = 0
+    if block_tables is not None:
+        bt_stride = int(block_tables.shape[-1])
+        if subpage_tables is None:
+            subpage_tables = torch.empty((W, B, subpage_stride), dtype=torch.int32, device=dev)
+    _check(lib().mla_shard_row_views(B, T, _ptr(qo_indptr, torch.int32, "qo_indptr"),
+                                     _ptr(row_len_global, torch.int32, "row_len_global"), W,
+                                     int(interleave), _ptr(row_len_local, torch.int32, "row_len_local"),
+                                     _ptr(block_tables, torch.int32, "block_tables"), bt_stride,
+                                     int(num_blocks), int(block_size),
+                                     _ptr(subpage_tables, torch.int32, "subpage_tables"),
+                                     int(subpage_stride), _stream(stream)), "mla_shard_row_views")
+    return row_len_local, subpage_tables
+
+
 def make_decode_args(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_, num_segments,
                      max_qlen, sm_scale, kv_scale=1.0, out=None, lse=None, flags=0,
-                     num_views=1) -> DecodeArgs:
+                     num_views=1, wait_cycles=0) -> DecodeArgs:
     T, H, dk = q.shape
     if dk != D_QK:
         raise ValueError("q must be [T, H, 576]")
@@ -231,6 +263,7 @@ def make_decode_args(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_,
     a.lse = _ptr(lse, torch.float32, "lse")
     a.flags = int(flags)
     a.num_views = int(num_views)
+    a.wait_cycles = int(wait_cycles)
     return a
 
 
@@ -240,13 +273,17 @@ def decode_verify_workspace_bytes(a: DecodeArgs) -> int:
 
 def decode_verify(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_, num_segments,
                   max_qlen, sm_scale, kv_scale=1.0, out=None, lse=None, workspace=None,
-                  stream=None, skip_merge=False, num_views=1, uniform_segments=False):
+                  stream=None, skip_merge=False, num_views=1, uniform_segments=False,
+                  wait_cycles=0, fused_merge=False):
     """mla_decode_verify.  Returns (out [T, H, 512] bf16, lse [T, H] f32, workspace).
     skip_merge: leave the segment partials in the workspace (MLA_DECODE_SKIP_MERGE).
     uniform_segments: the pages' equal split per request (MLA_DECODE_UNIFORM_SEGMENTS)
     instead of the balanced split.
     num_views V > 1: row_len [V, T], subpage_table [V, B, stride]; out [V, T, H, 512],
-    lse [V, T, H] (V row views of the same queries, one launch)."""
+    lse [V, T, H] (V row views of the same queries, one launch).
+    wait_cycles: bound on each in-kernel wait in SM cycles (0 = the library default).
+    fused_merge: merge the balanced split's parts inside the decode kernel
+    (MLA_DECODE_FUSED_MERGE) instead of a separate merge launch."""
     T, H, _ = q.shape
     V = max(1, int(num_views))
     lead = (V, T) if V > 1 else (T,)
@@ -257,7 +294,9 @@ def decode_verify(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_, nu
     a = make_decode_args(q, kv_cache, qo_indptr, row_len, subpage_table, page_size_,
                          num_segments, max_qlen, sm_scale, kv_scale, out, lse,
                          (MLA_DECODE_SKIP_MERGE if skip_merge else 0) |
-                         (MLA_DECODE_UNIFORM_SEGMENTS if uniform_segments else 0), num_views=V)
+                         (MLA_DECODE_UNIFORM_SEGMENTS if uniform_segments else 0) |
+                         (MLA_DECODE_FUSED_MERGE if fused_merge else 0), num_views=V,
+                         wait_cycles=wait_cycles)
     need = decode_verify_workspace_bytes(a)
     if need and (workspace is None or workspace.numel() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -274,9 +313,10 @@ def decode_verify_noalloc(q, kv_cache, qo_indptr, row_len, subpage_table, page_s
                           num_segments, max_qlen, sm_scale, kv_scale=1.0, out=None, lse=None,
                           stream=None):
     """mla_decode_verify_noalloc: the library's own static device scratch instead of a
-    caller workspace, for callers that cannot allocate device memory at the call (under
-    graph capture, fixed-budget serving runtimes, allocator-less C hosts).  Calls that
-    overlap on the GPU share that scratch and must be serialised.  Returns (out, lse)."""
+    caller workspace, for callers that cannot allocate device memory at the call (serving
+    runtimes that reserve all device memory at start-up, C or plugin hosts without a device
+    allocator).  Calls that overlap on the GPU share that scratch and must be serialised.
+    Returns (out, lse)."""
     T, H, _ = q.shape
     if out is None:
         out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=q.device)
@@ -314,20 +354,25 @@ def workspace_views(workspace: torch.Tensor, num_reqs: int, max_qlen: int, num_r
 
 
 def merge_segments(segm_out, segm_max, segm_sum, qo_indptr, max_qlen, out=None, lse=None,
-                   stream=None):
-    """mla_merge_segments, segment mode: bf16 partial blocks [B, RB, S, 8, 512, 8] (the
-    decode workspace layout) + [T, H, S] f32 base-2 stats; qo_indptr [B + 1] int32."""
-    T, H, S = segm_max.shape
+                   stream=None, num_views=1):
+    """mla_merge_segments, segment mode: bf16 partial blocks [V*B, RB, S, 8, 512, 8] (the
+    decode workspace layout) + [V*T, H, S] f32 base-2 stats; qo_indptr [B + 1] int32.
+    num_views V > 1: out [V, T, H, 512], lse [V, T, H] (the V row views of one decode)."""
+    VT, H, S = segm_max.shape
+    V = max(1, int(num_views))
+    T = VT // V
+    lead = (V, T) if V > 1 else (T,)
     if out is None:
-        out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=segm_out.device)
+        out = torch.empty((*lead, H, D_V), dtype=torch.bfloat16, device=segm_out.device)
     if lse is None:
-        lse = torch.empty((T, H), dtype=torch.float32, device=segm_out.device)
+        lse = torch.empty((*lead, H), dtype=torch.float32, device=segm_out.device)
     m = MergeArgs()
     m.mode, m.num_rows, m.num_heads, m.num_parts = MLA_MERGE_SEGMENTS, T, H, S
     m.segm_out = _ptr(segm_out, torch.bfloat16, "segm_out")
     m.qo_indptr = _ptr(qo_indptr, torch.int32, "qo_indptr")
     m.num_reqs = int(qo_indptr.shape[0]) - 1
     m.max_qlen = int(max_qlen)
+    m.num_views = V
     m.segm_max = _ptr(segm_max, torch.float32, "segm_max")
     m.segm_sum = _ptr(segm_sum, torch.float32, "segm_sum")
     m.out = _ptr(out, torch.bfloat16, "out")

@@ -5,8 +5,9 @@ tables, split-K workspace, shard partial states, outputs), sized by static
 bounds, so a step issues only library launches and can be captured in a CUDA
 graph.  Unsharded step: mla_plan_rows (+ sub-page expansion) ->
 mla_decode_verify (decode + segment merge).  Context-sharded step (W round-robin
-shards simulated on one device): mla_plan_rows (global windows) -> per shard
-mla_shard_row_view -> one mla_decode_verify over the W row views (num_views = W)
+shards simulated on one device): mla_plan_rows (global windows) -> the W shard
+row views in one mla_shard_row_views launch -> one mla_decode_verify over the
+W row views (num_views = W)
 into a [W, T, H, .] state buffer -> mla_merge_segments (state mode).
 """
 from __future__ import annotations
@@ -22,7 +23,8 @@ class VerifyStep:
     def __init__(self, *, num_reqs: int, num_rows: int, num_heads: int, max_qlen: int,
                  block_size: int, num_blocks: int, block_table_width: int, max_kv_len: int,
                  num_segments: int = 1, world_size: int = 1, kv_fp8: bool = False,
-                 interleave: int = 1, uniform_segments: bool = False, device="cuda"):
+                 interleave: int = 1, uniform_segments: bool = False, fused_merge: bool = False,
+                 device="cuda"):
         self.B, self.T, self.H = num_reqs, num_rows, num_heads
         self.max_qlen = max_qlen
         self.block_size = block_size
@@ -31,6 +33,7 @@ class VerifyStep:
         self.interleave = interleave
         self.S = num_segments
         self.uniform = uniform_segments  # the pages' equal split instead of the balanced one
+        self.fused = fused_merge         # merge the balanced split's parts inside the decode kernel
         self.P = mla.page_size(block_size)
         self.sp_stride = max(1, -(-max_kv_len // self.P))
         self.kv_fp8 = kv_fp8
@@ -47,11 +50,13 @@ class VerifyStep:
                                         dtype=torch.bfloat16, device=dev)
             self.part_lse = torch.empty((world_size, num_rows, num_heads), dtype=torch.float32,
                                         device=dev)
-        ws = 256  # scheduler state
+        a256 = lambda x: (x + 255) & ~255
+        ws = 256  # work counter
         if num_segments > 1:
             items = world_size * num_rows * num_heads * num_segments
-            blocks = world_size * num_reqs * mla.row_blocks(max_qlen, num_heads) * num_segments
-            ws += ((blocks * 512 * 64 * 2 + 255) & ~255) + 2 * ((items * 4 + 255) & ~255)
+            units = world_size * num_reqs * mla.row_blocks(max_qlen, num_heads)
+            blocks = units * num_segments
+            ws += a256(blocks * 512 * 64 * 2) + 2 * a256(items * 4) + a256(units * 4)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
 
     def __call__(self, q: torch.Tensor, kv_cache: torch.Tensor, seq_lens: torch.Tensor,
@@ -65,26 +70,26 @@ class VerifyStep:
             mla.decode_verify(q, kv_cache, qo_indptr, self.row_len, self.subpage[0], self.P,
                               self.S, self.max_qlen, sm_scale, kv_scale, out=self.out,
                               lse=self.lse, workspace=self.workspace, stream=stream,
-                              uniform_segments=self.uniform)
+                              uniform_segments=self.uniform, fused_merge=self.fused)
             return self.out, self.lse
         mla.plan_rows(seq_lens, qo_indptr, self.T, row_len=self.row_len, row_req=self.row_req,
                       stream=stream)
-        for r in range(self.W):
-            mla.shard_row_view(qo_indptr, self.row_len, self.W, r, self.interleave, block_tables[r],
-                               self.num_blocks, self.block_size, self.sp_stride,
-                               row_len_local=self.row_len_local[r],
-                               subpage_table=self.subpage[r], stream=stream)
+        # the W shard row views (one per simulated rank) in one launch
+        mla.shard_row_views(qo_indptr, self.row_len, self.W, self.interleave, block_tables,
+                            self.num_blocks, self.block_size, self.sp_stride,
+                            row_len_local=self.row_len_local, subpage_tables=self.subpage,
+                            stream=stream)
         # all W shard views in one decode launch, straight into the shard states
         mla.decode_verify(q, kv_cache, qo_indptr, self.row_len_local, self.subpage, self.P, self.S,
                           self.max_qlen, sm_scale, kv_scale, out=self.part_out, lse=self.part_lse,
                           workspace=self.workspace, stream=stream, num_views=self.W,
-                          uniform_segments=self.uniform)
+                          uniform_segments=self.uniform, fused_merge=self.fused)
         mla.merge_states(self.part_out, self.part_lse, out=self.out, lse=self.lse, stream=stream)
         return self.out, self.lse
 
 
 def step_for_workload(wl, device="cuda", num_segments: Optional[int] = None,
-                      uniform_segments: bool = False) -> VerifyStep:
+                      uniform_segments: bool = False, fused_merge: bool = False) -> VerifyStep:
     """A VerifyStep sized for a ``workloads.Workload``."""
     return VerifyStep(num_reqs=wl.num_reqs, num_rows=wl.num_rows, num_heads=wl.num_heads,
                       max_qlen=int(wl.qlens.max()), block_size=wl.block_size,
@@ -92,7 +97,8 @@ def step_for_workload(wl, device="cuda", num_segments: Optional[int] = None,
                       max_kv_len=wl.max_kv_len,
                       num_segments=wl.num_segments if num_segments is None else num_segments,
                       world_size=wl.world_size, kv_fp8=(wl.kv_dtype == "fp8"),
-                      interleave=wl.interleave, uniform_segments=uniform_segments, device=device)
+                      interleave=wl.interleave, uniform_segments=uniform_segments,
+                      fused_merge=fused_merge, device=device)
 
 
 def device_inputs(wl, device="cuda"):

@@ -76,6 +76,22 @@ def run_gpu(wl, num_segments=None, device="cuda", uniform_segments=False):
     return out, lse, step
 
 
+def run_gpu_partials(wl, device="cuda"):
+    """The workload's step (row plan + sub-page tables), then the decode alone
+    with MLA_DECODE_SKIP_MERGE into the step's workspace: every unit's
+    split-K partials and statistics stay there (the pages' two-step form),
+    whatever the default path merges in-kernel.  Returns the step."""
+    from mla_decode_speculative_gb300 import mla, runner
+    step = runner.step_for_workload(wl, device)
+    q, kv, seq, ind, bt = runner.device_inputs(wl, device)
+    step(q, kv, seq, ind, bt, wl.sm_scale, wl.kv_scale)
+    mla.decode_verify(q, kv, ind, step.row_len, step.subpage[0], step.P, step.S, step.max_qlen,
+                      wl.sm_scale, wl.kv_scale, out=step.out, lse=step.lse, workspace=step.workspace,
+                      skip_merge=True)
+    torch.cuda.synchronize()
+    return step
+
+
 def rows_to_blocks(x, qo_indptr, num_heads, row_blocks):
     """[T, H, S, 512] per-(row, head) partials -> the decode workspace's block
     layout [B, RB, S, 8, 512, 8] (a request's rows t * H + h, 64 per block;

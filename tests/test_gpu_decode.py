@@ -1,7 +1,9 @@
 """Decode / causal verify through the C ABI against the float64 oracle.
 
-Small workloads are compared on every (row, head); full-size configured
-workloads (in the launch configuration the benchmark times) on sampled pairs.
+Every (row, head) is compared, on small workloads and on the full-size
+configured workloads in the launch configuration the benchmark times (the
+qlen-4 verify over 1k-8k contexts, the fp8 cache with mixed qlen, and the
+8-way sharded 128k-context verify).
 """
 import math
 
@@ -10,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from parity import assert_close, balanced_parts, blocks_to_rows, oracle_reference, run_gpu, sample_pairs
+from parity import assert_close, balanced_parts, blocks_to_rows, oracle_reference, run_gpu, run_gpu_partials
 from mla_decode_speculative_gb300 import mla, runner, workloads
 
 pytestmark = pytest.mark.gpu
@@ -21,16 +23,6 @@ def _full_check(wl, what, num_segments=None, uniform=False):
     assert mla.get_device_error() == 0
     ref_o, ref_l = oracle_reference(wl)
     return assert_close(out, lse, ref_o, ref_l, what)
-
-
-def _sampled_check(wl, n, what, seed=0):
-    out, lse, _ = run_gpu(wl)
-    assert mla.get_device_error() == 0
-    sel = sample_pairs(wl, n, seed)
-    ref_o, ref_l = oracle_reference(wl, sel)
-    o = out[sel[:, 0], sel[:, 1]]
-    l = lse[sel[:, 0], sel[:, 1]]
-    return assert_close(o, l, ref_o, ref_l, what)
 
 
 # ------------------------------------------------------------------ small, every pair
@@ -182,7 +174,7 @@ def test_balanced_split_slots_and_merge(S):
     sum = 0), and merging the kernel's own bf16 partials in float64 gives the
     oracle's attention -- every visible token counted once."""
     wl = workloads.verify_mtp4_bf16(seed=11, batch=9, lo=40, hi=5000, num_segments=S)
-    out, lse, step = run_gpu(wl)
+    step = run_gpu_partials(wl)
     assert mla.get_device_error() == 0
     H, B = wl.num_heads, wl.num_reqs
     RB = mla.row_blocks(int(wl.qlens.max()), H)
@@ -218,14 +210,26 @@ def test_balanced_split_slots_and_merge(S):
     assert_close(torch.tensor(mo), torch.tensor(ml), ref_o, ref_l, f"merged kernel partials, S={S}")
 
 
-@pytest.mark.parametrize("S", [3, 16])
-def test_balanced_parts_match_oracle_slot_by_slot(S):
+def _multi_block_workload(S):
+    """64 heads x qlen 1-4 mixed: up to four 64-row blocks per request, so a
+    block's own rows can be shorter than its unit's tile count (parts with no
+    visible token for some rows) and blocks past a request's rows are empty
+    units."""
+    rng = np.random.default_rng(15)
+    L = rng.integers(40, 2500, 7)
+    ql = rng.integers(1, 5, 7)
+    return workloads.make_workload("multi_block", L, ql, 64, 64, num_segments=S, seed=15)
+
+
+@pytest.mark.parametrize("S,shape", [(3, "verify"), (16, "verify"), (4, "multi_block"), (9, "multi_block")])
+def test_balanced_parts_match_oracle_slot_by_slot(S, shape):
     """Every part of the balanced split against the oracle's partial over the
     part's token range (the rule restated above): same empty slots, the
     normalised part output to the output tolerance, the part's log-sum-exp to
     the LSE tolerance."""
-    wl = workloads.verify_mtp4_bf16(seed=14, batch=6, lo=40, hi=3000, num_segments=S)
-    out, lse, step = run_gpu(wl)
+    wl = (workloads.verify_mtp4_bf16(seed=14, batch=6, lo=40, hi=3000, num_segments=S)
+          if shape == "verify" else _multi_block_workload(S))
+    step = run_gpu_partials(wl)
     assert mla.get_device_error() == 0
     H, B, Q = wl.num_heads, wl.num_reqs, int(wl.qlens.max())
     RB = mla.row_blocks(Q, H)
@@ -292,7 +296,7 @@ def test_static_bound_does_not_change_results():
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
 
 
-# ------------------------------------------------------------------ full-size, sampled
+# ------------------------------------------------------------------ full size, every pair
 
 def test_repeated_steps_are_bit_identical():
     """Each work item is computed start to finish by one CTA in a fixed
@@ -322,14 +326,115 @@ def test_repeated_steps_are_bit_identical():
         assert_close(first[0], first[1], ref_o, ref_l, wl.name)
 
 
-def test_verify_mtp4_full_size_sampled():
-    _sampled_check(workloads.verify_mtp4_bf16(), 96, "verify qlen=4 batch 32 L 1k-8k S=16")
+def test_verify_mtp4_full_size_every_pair():
+    _full_check(workloads.verify_mtp4_bf16(), "verify qlen=4 batch 32 L 1k-8k S=16")
 
 
-def test_fp8_full_size_sampled():
-    _sampled_check(workloads.fp8_mixed_qlen(), 96, "fp8 batch 64 L 512-32k")
+def test_fp8_full_size_every_pair():
+    _full_check(workloads.fp8_mixed_qlen(), "fp8 batch 64 L 512-32k")
 
 
-def test_dcp8_full_size_sampled():
-    wl = workloads.dcp8_verify_bf16(device="cuda")
-    _sampled_check(wl, 24, "dcp8 batch 16 context 128k")
+def test_dcp8_full_size_every_pair():
+    _full_check(workloads.dcp8_verify_bf16(device="cuda"), "dcp8 batch 16 context 128k")
+
+
+# ------------------------------------------------------------------ in-kernel split-K merge
+
+FUSED_CASES = {
+    # the configured qlen-4 verify and the 8-way sharded 128k-context verify
+    "verify_mtp4": lambda: workloads.verify_mtp4_bf16(),
+    "dcp8": lambda: workloads.dcp8_verify_bf16(device="cuda"),
+    # one long request cut into 14 chunks: a unit with more parts than the
+    # eight 64-dim output blocks, so some holders merge nothing
+    "one_long_request": lambda: workloads.make_workload("fused_long", [100000], [4], 16, 64,
+                                                        num_segments=16, seed=41, device="cuda"),
+    # many short requests: most units lie inside one chunk (out written
+    # straight from the accumulator), the rest span two
+    "many_short": lambda: workloads.make_workload(
+        "fused_short", np.random.default_rng(42).integers(64, 900, 100), [2] * 100, 16, 64,
+        num_segments=4, seed=42),
+    # four shard views in one launch, several row blocks per request
+    "views_row_blocks": lambda: workloads.make_workload("fused_views", [7000, 300, 12000], [4, 3, 8], 32, 64,
+                                                        world_size=4, num_segments=6, seed=43),
+    "fp8": lambda: workloads.fp8_mixed_qlen(seed=44, batch=20, lo=200, hi=20000, num_segments=8),
+    # sweep corner: 128 heads x qlen 8, 16 row blocks per request
+    "wide_rows": lambda: workloads.make_workload("fused_wide", [9000, 12000, 7000], [8, 8, 8], 128, 64,
+                                                 num_segments=8, seed=46, device="cuda"),
+}
+
+
+def _fused_and_two_step(wl):
+    """(fused out, fused lse, two-step out, two-step lse) for every view of a
+    workload whose row plan / shard views are prepared by its step."""
+    step = runner.step_for_workload(wl, "cuda")
+    q, kv, seq, ind, bt = runner.device_inputs(wl, "cuda")
+    step(q, kv, seq, ind, bt, wl.sm_scale, wl.kv_scale)
+    W, Q = wl.world_size, step.max_qlen
+    row_len = step.row_len if W == 1 else step.row_len_local
+    sp = step.subpage[0] if W == 1 else step.subpage
+    fo, fl, _ = mla.decode_verify(q, kv, ind, row_len, sp, step.P, step.S, Q, wl.sm_scale, wl.kv_scale,
+                                  num_views=W, fused_merge=True)
+    two_o, two_l, ws = mla.decode_verify(q, kv, ind, row_len, sp, step.P, step.S, Q, wl.sm_scale,
+                                         wl.kv_scale, skip_merge=True, num_views=W)
+    so, sm, ss = mla.workspace_views(ws, wl.num_reqs, Q, wl.num_rows, wl.num_heads, step.S, num_views=W)
+    mla.merge_segments(so, sm, ss, ind, Q, out=two_o, lse=two_l, num_views=W)
+    torch.cuda.synchronize()
+    return fo, fl, two_o, two_l
+
+
+@pytest.mark.parametrize("case", sorted(FUSED_CASES))
+def test_fused_merge_matches_oracle_and_two_step_form(case):
+    """MLA_DECODE_FUSED_MERGE merges the balanced split's parts inside the
+    decode kernel (single-chunk units straight from the accumulator; the last
+    arriving part's SM, helped by holders that wait for the unit, for the
+    rest); its out / LSE must match the oracle and the pages' two-step form
+    (decode with MLA_DECODE_SKIP_MERGE, then mla_merge_segments) within the
+    stated tolerances, view by view."""
+    wl = FUSED_CASES[case]()
+    fo, fl, two_o, two_l = _fused_and_two_step(wl)
+    assert mla.get_device_error() == 0
+    row_len, _, _ = oracle.plan_rows(wl.seq_lens, wl.qo_indptr)
+    kvh, qb = wl.kv_host(), wl.q_bits()
+    for r in range(wl.world_size):
+        local = oracle.shard_row_view(row_len, wl.world_size, r, wl.interleave) if wl.world_size > 1 else row_len
+        ref_o, ref_l = oracle.attention(wl.qo_indptr, local, qb, kvh, wl.kv_scale, wl.sm_scale,
+                                        wl.block_tables[r], wl.block_size)
+        f = (fo[r], fl[r]) if wl.world_size > 1 else (fo, fl)
+        t = (two_o[r], two_l[r]) if wl.world_size > 1 else (two_o, two_l)
+        assert_close(f[0], f[1], ref_o, ref_l, f"{case}: in-kernel merge, view {r}")
+        assert_close(t[0], t[1], ref_o, ref_l, f"{case}: two-step, view {r}")
+
+
+def test_fused_merge_repeated_launches_are_bit_identical():
+    """Which holder merges which output block depends on arrival order, but
+    every block is merged from the same published parts in the same order,
+    so repeated launches agree bit for bit."""
+    wl = workloads.verify_mtp4_bf16(seed=45, batch=12, lo=500, hi=9000, num_segments=16)
+    step = runner.step_for_workload(wl, "cuda")
+    q, kv, seq, ind, bt = runner.device_inputs(wl, "cuda")
+    step(q, kv, seq, ind, bt, wl.sm_scale)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+    first = None
+    for it in range(30):
+        if it % 4 == 0:
+            flush.fill_(float(it))
+        out, lse, _ = mla.decode_verify(q, kv, ind, step.row_len, step.subpage[0], step.P, step.S,
+                                        step.max_qlen, wl.sm_scale, workspace=step.workspace,
+                                        fused_merge=True)
+        if first is None:
+            first = (out.clone(), lse.clone())
+        else:
+            assert torch.equal(out, first[0]) and torch.equal(lse, first[1]), f"launch {it} differs"
+    assert mla.get_device_error() == 0
+
+
+def test_fused_merge_needs_the_balanced_split():
+    wl = workloads.verify_mtp4_bf16(seed=47, batch=3, lo=300, hi=900, num_segments=4)
+    step = runner.step_for_workload(wl, "cuda")
+    q, kv, seq, ind, bt = runner.device_inputs(wl, "cuda")
+    step(q, kv, seq, ind, bt, wl.sm_scale)
+    for kw in (dict(uniform_segments=True), dict(skip_merge=True)):
+        with pytest.raises(mla.MLAError) as e:
+            mla.decode_verify(q, kv, ind, step.row_len, step.subpage[0], step.P, 4, 4, wl.sm_scale,
+                              fused_merge=True, **kw)
+        assert e.value.status == mla.MLA_ERR_UNSUPPORTED

@@ -137,3 +137,44 @@ def test_device_checks_fire_without_faulting():
     # bad indptr (decreasing)
     mla.plan_rows(_dev([10, 10]), _dev([0, 3, 2]), 3)
     assert mla.get_device_error() in (1, 2)
+
+
+@pytest.mark.parametrize("W,I", [(8, 1), (3, 4), (2, 64)])
+def test_all_shard_views_in_one_launch_bit_exact(W, I):
+    """mla_shard_row_views computes every rank's view in one launch: each view
+    equals the oracle's shard row view and sub-page table, and the per-rank
+    call mla_shard_row_view, bit for bit."""
+    rng = np.random.default_rng(70 + W * 7 + I)
+    B = 17
+    seq = rng.integers(1, 7000, B).astype(np.int32)
+    ql = np.minimum(rng.integers(1, 9, B), seq).astype(np.int32)
+    ind = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    T = int(ind[-1])
+    o_rl, _, _ = oracle.plan_rows(seq, ind)
+    rl, _, _ = mla.plan_rows(_dev(seq), _dev(ind), T)
+    block_size = 16
+    P = oracle.page_size(block_size)
+    cap = [-(-int(L) // (W * I)) * I for L in seq]
+    nb = [-(-c // block_size) for c in cap]
+    num_blocks = W * sum(nb) + 3
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    bts = np.full((W, B, max(nb)), -1, np.int32)
+    pos = 0
+    for r in range(W):
+        for b in range(B):
+            bts[r, b, :nb[b]] = perm[pos:pos + nb[b]]
+            pos += nb[b]
+    width = -(-max(cap) // P) + 1
+    loc, sp = mla.shard_row_views(_dev(ind), rl, W, I, _dev(bts), num_blocks, block_size, width)
+    assert mla.get_device_error() == 0
+    loc, sp = loc.cpu().numpy(), sp.cpu().numpy()
+    total = np.zeros(T, np.int64)
+    for r in range(W):
+        o_loc = oracle.shard_row_view(o_rl, W, r, I)
+        assert (loc[r] == o_loc).all(), r
+        kv_len = np.array([o_loc[ind[b]:ind[b + 1]].max() for b in range(B)], np.int32)
+        assert (sp[r] == oracle.subpage_table(kv_len, bts[r], num_blocks, block_size, width)).all(), r
+        one_loc, one_sp = mla.shard_row_view(_dev(ind), rl, W, r, I, _dev(bts[r]), num_blocks, block_size, width)
+        assert (one_loc.cpu().numpy() == loc[r]).all() and (one_sp.cpu().numpy() == sp[r]).all()
+        total += o_loc
+    assert (total == o_rl).all()

@@ -1,7 +1,13 @@
 """Sweep points (heads {16,64,128}, batch 1-256, context 4k-132k, qlen
-{1,2,4,8}, bf16/fp8, block {16,64,256}) through the C ABI, checked against the
-oracle on sampled (row, head) pairs.  Total visible tokens per point are capped
-so the suite stays quick; the corners of each factor are covered explicitly."""
+{1,2,4,8}, bf16/fp8, block {16,64,256}) through the C ABI against the oracle.
+
+The seeded grid's points run the direct path (one segment) with their total
+visible tokens capped so the suite stays quick, every factor value at least
+once, checked on sampled (row, head) pairs.  The corners run the default
+balanced split-K (several segment slots) at full size and are checked on
+every (row, head): the widest rows (128 heads x qlen 8 = 16 row blocks per
+request), 16-token pages at 64k+ contexts, and an fp8 cache with 256-token
+blocks (128-row sub-pages spanning two tiles)."""
 import numpy as np
 import pytest
 
@@ -33,3 +39,24 @@ def test_sweep_point_sampled(pt):
     sel = sample_pairs(wl, 48, seed=pt.seed)
     ref_o, ref_l = oracle_reference(wl, sel)
     assert_close(out[sel[:, 0], sel[:, 1]], lse[sel[:, 0], sel[:, 1]], ref_o, ref_l, pt.name())
+
+
+# balanced split-K at the sweep's corners, full size, every (row, head)
+SPLIT_CORNERS = [
+    (workloads.SweepPoint(128, 6, 12000, 8, "bf16", 64, 911), 8),     # 16 row blocks per request
+    (workloads.SweepPoint(64, 3, 20000, 2, "fp8", 64, 912), 6),       # 2 row blocks, fp8
+    (workloads.SweepPoint(16, 3, 70000, 4, "bf16", 16, 913), 4),      # 16-token pages, 64k+ context
+    (workloads.SweepPoint(16, 4, 40000, 3, "fp8", 256, 914), 8),      # fp8, 128-row sub-pages
+]
+
+
+@pytest.mark.parametrize("pt,S", SPLIT_CORNERS, ids=lambda x: x.name() if hasattr(x, "name") else f"S{x}")
+def test_sweep_corner_balanced_split_every_pair(pt, S):
+    g = np.random.default_rng(pt.seed)
+    L = g.integers(max(pt.qlen, pt.context // 2), pt.context + 1, pt.batch)
+    wl = workloads.make_workload(pt.name() + f"_s{S}", L, [pt.qlen] * pt.batch, pt.heads, pt.block_size,
+                                 pt.kv_dtype, 1, S, pt.seed, device="cuda")
+    out, lse, _ = run_gpu(wl)
+    assert mla.get_device_error() == 0
+    ref_o, ref_l = oracle_reference(wl)
+    assert_close(out, lse, ref_o, ref_l, wl.name)

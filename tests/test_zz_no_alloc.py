@@ -1,10 +1,9 @@
 """The allocation-free entry point (mla_decode_verify_noalloc) against the
 workspace entry point (mla_decode_verify) through the C ABI.
 
-It serves callers that cannot allocate device memory where they call -- code
-under CUDA-graph capture, serving runtimes with a fixed memory budget, C
-hosts without a device allocator -- by using a static scratch array inside the
-library.  Two calls in a row must both match the workspace path within the
+It serves callers that cannot allocate device memory where they call --
+serving runtimes with a fixed memory budget, C hosts without a device
+allocator -- by using a static scratch array inside the library.  Two calls in a row must both match the workspace path within the
 tolerance the parity tests use, and oversize problems are refused before any
 launch.  This file sorts last so a stopping run has covered everything else."""
 import numpy as np
