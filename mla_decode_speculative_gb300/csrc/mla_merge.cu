@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -37,7 +38,6 @@ namespace {
 
 constexpr int kThreadsPerItem = 128;  // state mode: 512 dims / 4 per thread
 constexpr int kBlockRows = 64;        // segment mode: rows per partial block
-constexpr int kDimsPerCta = 64;       // segment mode: output dims per CTA
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct StateParams {
@@ -82,22 +82,47 @@ __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x 
 
 // ---------------------------------------------------------------- segments
 constexpr int kSegChunk = 32;  // segments whose weights are staged at a time
-constexpr int kSegBatch = 8;   // live segments whose partial blocks are read at a time
 
-// grid (V * B * RB, 512 / 64), 256 threads: one (view, request, row block)
-// unit x 64 output dims.  The unit's 64 rows x S statistics are contiguous:
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void *gptr) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Shape of one segment-merge CTA: kD output dims of one unit, 256 threads,
+// live parts streamed through a ring of kRing slices in shared memory.
+template <int kD>
+struct SegShape {
+  static constexpr int G = 256 / kD;             // row groups: thread t takes rows of group t / kD
+  static constexpr int OPT = 8 / G;              // row octets per thread
+  static constexpr int SLICE = 8 * kD * 16;      // bytes of one part's slice: [octet][dim] x 16 B
+  static constexpr int RING = kD == 256 ? 6 : (kD == 128 ? 5 : 4);
+  static constexpr int CTAS = kD == 256 ? 1 : (kD == 128 ? 2 : 4);  // per SM
+  static constexpr int DYN = RING * SLICE;       // dynamic shared memory
+};
+
+// grid (V * B * RB, 512 / kD), 256 threads: one (view, request, row block)
+// unit x kD output dims.  The unit's 64 rows x S statistics are contiguous:
 // one pass gives every row its max and denominator (four threads per row,
 // each a running pair rescaled as its max grows) and keeps the maxima of the
 // first 32 segments in shared memory; the normalised weights 2^(m_s - M) / den
-// of 32 segments at a time are then formed there, the segments with a
-// non-zero weight listed, and their partial blocks read eight at a time.
-// Warp w takes dims 8w .. 8w+7 of the CTA's 64, lane l dim 8w + l % 8 for the
-// row octets l / 8 and l / 8 + 4: every load instruction of a warp covers
-// four whole 128-byte runs (eight consecutive dims of one octet).
-__global__ void __launch_bounds__(256, 2) merge_segment_blocks(const SegParams p) {
+// of 32 segments at a time are then formed there and the segments with a
+// non-zero weight listed.  Their slices ([octet][dim] of the kD dims, whole
+// 16-byte pieces of 8 rows) stream through a ring of kRing shared-memory
+// slots with cp.async (a slot per commit group, kRing - 1 slices in flight),
+// so a CTA keeps up to (kRing - 1) x 8 x kD x 16 bytes of reads in flight
+// without holding them in registers.  Thread t accumulates dim t % kD for the
+// rows of its row octets; the merged tile leaves through shared memory as
+// 16-byte row pieces.
+template <int kD>
+__global__ void __launch_bounds__(256, SegShape<kD>::CTAS) merge_segment_stream(const SegParams p) {
+  using Sh = SegShape<kD>;
+  extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(16) float s_m[kSegChunk][kBlockRows];
   __shared__ __align__(16) float s_w[kSegChunk][kBlockRows];
-  __shared__ __align__(16) uint16_t s_o[kBlockRows][kDimsPerCta + 8];  // bf16 [row][dim], padded rows
   __shared__ float s_part[4][kBlockRows], s_dpart[4][kBlockRows];
   __shared__ int s_live[kSegChunk], s_list[kSegChunk], s_nlive;
   __shared__ float s_M[kBlockRows], s_inv[kBlockRows];
@@ -114,6 +139,7 @@ __global__ void __launch_bounds__(256, 2) merge_segment_blocks(const SegParams p
   const int64_t grow0 = (static_cast<int64_t>(v) * p.num_rows + q0) * p.num_heads + rb * kBlockRows;  // first row
   const float *mx = p.segm_max + grow0 * S;  // [64 rows][S], contiguous
   const float *sm = p.segm_sum + grow0 * S;
+  const int dim0 = blockIdx.y * kD;
 
   const int row = tid & (kBlockRows - 1), quarter = tid >> 6;
   float Mq = -INFINITY, dq = 0.0f;
@@ -162,12 +188,21 @@ __global__ void __launch_bounds__(256, 2) merge_segment_blocks(const SegParams p
   }
   __syncthreads();
 
-  const int dim = blockIdx.y * kDimsPerCta + warp * 8 + (lane & 7);
-  const int og = lane >> 3;  // row octets og and og + 4
-  float a[16];               // rows 8 og + k (k < 8) and 8 (og + 4) + k - 8
+  const int dl = tid % kD, grp = tid / kD;
+  float a[Sh::OPT * 8];  // rows 8 (grp * OPT + o) + k
 #pragma unroll
-  for (int k = 0; k < 16; ++k) a[k] = 0.0f;
+  for (int k = 0; k < Sh::OPT * 8; ++k) a[k] = 0.0f;
   const int64_t blk0 = (static_cast<int64_t>(vb) * p.row_blocks + rb) * S;
+  const uint32_t s_ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+  // issue the copies of one live slice into ring slot `slot`
+  auto issue = [&](int sc, int slot) {
+    const uint4 *blk = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + sc) * (512 * kBlockRows));
+#pragma unroll
+    for (int j = 0; j < 8 * kD / 256; ++j) {
+      const int c = tid + 256 * j, o = c / kD, d = c % kD;
+      cp_async16(s_ring + slot * Sh::SLICE + c * 16, blk + o * 512 + dim0 + d);
+    }
+  };
   for (int c0 = 0; c0 < S; c0 += kSegChunk) {
     const int nc = min(kSegChunk, S - c0);
     // normalised weights of this chunk (0 for empty rows / segments / padding rows)
@@ -192,53 +227,53 @@ __global__ void __launch_bounds__(256, 2) merge_segment_blocks(const SegParams p
     }
     __syncthreads();
     const int n_live = s_nlive;
-    for (int i0 = 0; i0 < n_live; i0 += kSegBatch) {
-      uint4 x[kSegBatch][2];
+    // ring: slices i .. i + RING - 2 in flight while slice i is summed
 #pragma unroll
-      for (int u = 0; u < kSegBatch; ++u) {
-        if (i0 + u < n_live) {
-          const uint4 *blk = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + c0 + s_list[i0 + u]) * (512 * kBlockRows));
-          x[u][0] = __ldcs(blk + og * 512 + dim);
-          x[u][1] = __ldcs(blk + (og + 4) * 512 + dim);
-        }
-      }
-      // a weight of 0 selects 0: an empty row's slot is never used as a value
-#pragma unroll
-      for (int u = 0; u < kSegBatch; ++u) {
-        if (i0 + u >= n_live) break;
-        const int sc = s_list[i0 + u];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float4 wa = *reinterpret_cast<const float4 *>(&s_w[sc][8 * (og + 4 * h)]);
-          const float4 wb = *reinterpret_cast<const float4 *>(&s_w[sc][8 * (og + 4 * h) + 4]);
-          const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-          const uint32_t vv[4] = {x[u][h].x, x[u][h].y, x[u][h].z, x[u][h].w};
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float e = (k & 1) ? bf16_hi(vv[k >> 1]) : bf16_lo(vv[k >> 1]);
-            a[8 * h + k] += (w[k] != 0.0f) ? w[k] * e : 0.0f;
-          }
-        }
-      }
+    for (int i = 0; i < Sh::RING - 1; ++i) {
+      if (i < n_live) issue(c0 + s_list[i], i);
+      cp_async_commit();
     }
+    for (int i = 0; i < n_live; ++i) {
+      if (i + Sh::RING - 1 < n_live) issue(c0 + s_list[i + Sh::RING - 1], (i + Sh::RING - 1) % Sh::RING);
+      cp_async_commit();
+      cp_async_wait<Sh::RING - 1>();  // this thread's copies of slice i have landed
+      __syncthreads();                 // ... and every thread's
+      const uint4 *slot = reinterpret_cast<const uint4 *>(ring + (i % Sh::RING) * Sh::SLICE);
+      const int sc = s_list[i];
+#pragma unroll
+      for (int o = 0; o < Sh::OPT; ++o) {
+        const int oc = grp * Sh::OPT + o;
+        const uint4 x = slot[oc * kD + dl];
+        const float4 wa = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oc]);
+        const float4 wb = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oc + 4]);
+        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        const uint32_t vv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // a weight of 0 selects 0: an empty row's slot is never a value
+          const float e = (k & 1) ? bf16_hi(vv[k >> 1]) : bf16_lo(vv[k >> 1]);
+          a[8 * o + k] += (w[k] != 0.0f) ? w[k] * e : 0.0f;
+        }
+      }
+      __syncthreads();  // slot i % RING is refilled by the next iteration
+    }
+    cp_async_wait<0>();
     __syncthreads();  // s_w / s_live are refilled by the next chunk
   }
-  // transpose through shared memory: this thread's dim for rows 8 og + k and 8 (og + 4) + k
+  // [row][dim] through shared memory (the ring is free now), then 16-byte row pieces
+  uint16_t *s_o = reinterpret_cast<uint16_t *>(ring);  // [64][kD + 8]
 #pragma unroll
-  for (int h = 0; h < 2; ++h)
+  for (int o = 0; o < Sh::OPT; ++o)
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const __nv_bfloat16 hv = __float2bfloat16_rn(a[8 * h + k]);
-      s_o[8 * (og + 4 * h) + k][warp * 8 + (lane & 7)] = *reinterpret_cast<const uint16_t *>(&hv);
+      const __nv_bfloat16 hv = __float2bfloat16_rn(a[8 * o + k]);
+      s_o[(8 * (grp * Sh::OPT + o) + k) * (kD + 8) + dl] = *reinterpret_cast<const uint16_t *>(&hv);
     }
   __syncthreads();
-  // 64 rows x 128 bytes: thread t writes 16-byte pieces t and t + 256
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int i = tid + 256 * h, r = i >> 3, c16 = i & 7;
+  for (int i = tid; i < kBlockRows * kD / 8; i += 256) {
+    const int r = i / (kD / 8), c16 = i % (kD / 8);
     if (r < n_rows) {
-      const uint4 val = *reinterpret_cast<const uint4 *>(&s_o[r][8 * c16]);
-      *reinterpret_cast<uint4 *>(p.out + (grow0 + r) * 512 + blockIdx.y * kDimsPerCta + 8 * c16) = val;
+      const uint4 val = *reinterpret_cast<const uint4 *>(&s_o[r * (kD + 8) + 8 * c16]);
+      *reinterpret_cast<uint4 *>(p.out + (grow0 + r) * 512 + dim0 + 8 * c16) = val;
     }
   }
 }
@@ -402,6 +437,10 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_states(const StateParam
   if (tid == 0) p.lse[it] = M + logf(den);
 }
 
+// Per device: the streaming merges' shared-memory attributes are set (relaxed
+// atomics: concurrent first calls store the same value).
+std::atomic<bool> g_seg_attr_set[64];
+
 }  // namespace
 
 mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
@@ -424,7 +463,29 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
       set_error("mla_merge_segments: bad row-block count (%lld)", (long long)ctas);
       return MLA_ERR_UNSUPPORTED;
     }
-    merge_segment_blocks<<<dim3(static_cast<unsigned>(ctas), 512 / kDimsPerCta), 256, 0, stream>>>(p);
+    // dims per CTA: 128 (two CTAs per SM), or 64 (four) when there are too
+    // few units to give every SM two CTAs
+    int dev = 0, sms = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "merge: SM count");
+    if (dev < 0 || dev >= 64) {
+      set_error("device ordinal %d out of range", dev);
+      return MLA_ERR_CUDA;
+    }
+    if (!g_seg_attr_set[dev].load(std::memory_order_relaxed)) {
+      e0 = cudaFuncSetAttribute(merge_segment_stream<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SegShape<128>::DYN);
+      if (e0 == cudaSuccess)
+        e0 = cudaFuncSetAttribute(merge_segment_stream<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  SegShape<64>::DYN);
+      if (e0 != cudaSuccess) return cuda_fail(e0, "cudaFuncSetAttribute(merge smem)");
+      g_seg_attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    if (ctas * (512 / 128) >= 2LL * 2 * sms)
+      merge_segment_stream<128><<<dim3(static_cast<unsigned>(ctas), 512 / 128), 256, SegShape<128>::DYN, stream>>>(p);
+    else
+      merge_segment_stream<64><<<dim3(static_cast<unsigned>(ctas), 512 / 64), 256, SegShape<64>::DYN, stream>>>(p);
   } else {
     StateParams p{};
     p.part_out = static_cast<const __nv_bfloat16 *>(m.part_out);
