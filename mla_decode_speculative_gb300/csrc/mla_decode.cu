@@ -657,10 +657,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   const bool balanced = p.balanced != 0;
-  // Balanced split: the producer's one chunk claim, issued now so that its
-  // round trip overlaps the unit table below.
-  int first_claim = 0;
-  if (balanced && warp == kProducerWarp && lane == 0) first_claim = atomicAdd(p.sched, 1);
+  // Balanced split: the producer's one chunk.  With the merge in this kernel
+  // it is claimed from the work counter (a holder waits only for chunks that
+  // running CTAs have claimed), the claim issued now so that its round trip
+  // overlaps the unit table below; otherwise CTA c takes chunk c (every
+  // chunk has a CTA: there are at most as many chunks as CTAs).
+  int first_claim = static_cast<int>(blockIdx.x);
+  if (kFused && balanced && warp == kProducerWarp && lane == 0) first_claim = atomicAdd(p.sched, 1);
   if (balanced) {
     // tiles of every (view, request, row block) unit: the request's longest
     // visible length in 64-token tiles, 0 for a row block without rows

@@ -98,9 +98,9 @@ template <int kD>
 struct SegShape {
   static constexpr int G = 256 / kD;             // row groups: thread t takes rows of group t / kD
   static constexpr int OPT = 8 / G;              // row octets per thread
-  static constexpr int SLICE = 8 * kD * 16;      // bytes of one part's slice: [octet][dim] x 16 B
-  static constexpr int RING = kD == 256 ? 6 : (kD == 128 ? 5 : 4);
-  static constexpr int CTAS = kD == 256 ? 1 : (kD == 128 ? 2 : 4);  // per SM
+  static constexpr int SLICE = 8 * kD * 16;      // bytes of one part's slice (kD dims x 8 octets x 16 B)
+  static constexpr int RING = kD == 128 ? 5 : 6;
+  static constexpr int CTAS = kD == 128 ? 2 : 3;  // per SM
   static constexpr int DYN = RING * SLICE;       // dynamic shared memory
 };
 
@@ -110,13 +110,15 @@ struct SegShape {
 // each a running pair rescaled as its max grows) and keeps the maxima of the
 // first 32 segments in shared memory; the normalised weights 2^(m_s - M) / den
 // of 32 segments at a time are then formed there and the segments with a
-// non-zero weight listed.  Their slices ([octet][dim] of the kD dims, whole
-// 16-byte pieces of 8 rows) stream through a ring of kRing shared-memory
-// slots with cp.async (a slot per commit group, kRing - 1 slices in flight),
+// non-zero weight listed.  Thread t sums dim t % kD for the rows of its row
+// octets: the 16-byte (8-row) pieces of those octets of every live part
+// stream through the thread's own slots of a kRing-deep ring in shared
+// memory with cp.async (a commit group per part, kRing - 1 parts in flight),
 // so a CTA keeps up to (kRing - 1) x 8 x kD x 16 bytes of reads in flight
-// without holding them in registers.  Thread t accumulates dim t % kD for the
-// rows of its row octets; the merged tile leaves through shared memory as
-// 16-byte row pieces.
+// without holding them in registers, and since every thread reads back only
+// the pieces it copied itself, no barrier is needed inside the stream.  A
+// warp's copy covers 32 consecutive dims of one octet, whole 128-byte runs.
+// The merged tile leaves through shared memory as 16-byte row pieces.
 template <int kD>
 __global__ void __launch_bounds__(256, SegShape<kD>::CTAS) merge_segment_stream(const SegParams p) {
   using Sh = SegShape<kD>;
@@ -141,6 +143,32 @@ __global__ void __launch_bounds__(256, SegShape<kD>::CTAS) merge_segment_stream(
   const float *sm = p.segm_sum + grow0 * S;
   const int dim0 = blockIdx.y * kD;
 
+  const int dl = tid % kD, grp = tid / kD;
+  float a[Sh::OPT * 8];  // rows 8 (grp * OPT + o) + k
+#pragma unroll
+  for (int k = 0; k < Sh::OPT * 8; ++k) a[k] = 0.0f;
+  const int64_t blk0 = (static_cast<int64_t>(vb) * p.row_blocks + rb) * S;
+  const uint32_t s_ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+  // this thread's pieces of part `sc` into its own places in ring slot `slot`:
+  // slot [256 threads][OPT] x 16 B
+  auto issue = [&](int sc, int slot) {
+    const uint4 *blk = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + sc) * (512 * kBlockRows));
+#pragma unroll
+    for (int o = 0; o < Sh::OPT; ++o)
+      cp_async16(s_ring + slot * Sh::SLICE + (o * 256 + tid) * 16, blk + (grp * Sh::OPT + o) * 512 + dim0 + dl);
+  };
+  // The first two segment slots are copied before the statistics are known
+  // (a request's first slots hold its tokens; a slot that turns out empty
+  // just gets weight 0, which selects 0), so that the statistics' round trip
+  // overlaps the first data copies; the ring's other slots start after it.
+  constexpr int kPre = 2;
+  static_assert(kPre <= Sh::RING - 1, "prefetched slots fit the ring");
+  const int n_pre = min(kPre, S);
+#pragma unroll
+  for (int i = 0; i < Sh::RING - 1; ++i) {
+    if (i < n_pre) issue(i, i);
+    if (i < kPre) cp_async_commit();
+  }
   const int row = tid & (kBlockRows - 1), quarter = tid >> 6;
   float Mq = -INFINITY, dq = 0.0f;
   auto take = [&](float m, float l) {
@@ -188,21 +216,6 @@ __global__ void __launch_bounds__(256, SegShape<kD>::CTAS) merge_segment_stream(
   }
   __syncthreads();
 
-  const int dl = tid % kD, grp = tid / kD;
-  float a[Sh::OPT * 8];  // rows 8 (grp * OPT + o) + k
-#pragma unroll
-  for (int k = 0; k < Sh::OPT * 8; ++k) a[k] = 0.0f;
-  const int64_t blk0 = (static_cast<int64_t>(vb) * p.row_blocks + rb) * S;
-  const uint32_t s_ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-  // issue the copies of one live slice into ring slot `slot`
-  auto issue = [&](int sc, int slot) {
-    const uint4 *blk = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + sc) * (512 * kBlockRows));
-#pragma unroll
-    for (int j = 0; j < 8 * kD / 256; ++j) {
-      const int c = tid + 256 * j, o = c / kD, d = c % kD;
-      cp_async16(s_ring + slot * Sh::SLICE + c * 16, blk + o * 512 + dim0 + d);
-    }
-  };
   for (int c0 = 0; c0 < S; c0 += kSegChunk) {
     const int nc = min(kSegChunk, S - c0);
     // normalised weights of this chunk (0 for empty rows / segments / padding rows)
@@ -219,31 +232,33 @@ __global__ void __launch_bounds__(256, SegShape<kD>::CTAS) merge_segment_stream(
       if (w != 0.0f) s_live[sc] = 1;
     }
     __syncthreads();
-    if (warp == 0) {  // the chunk's live slots, in order
-      const bool lv = lane < nc && s_live[lane] != 0;
+    const int pre = c0 == 0 ? n_pre : 0;  // slots already in the ring, live or not
+    if (warp == 0) {  // the slots to sum, in order: the prefetched ones, then the other live ones
+      const bool lv = lane < nc && (lane < pre || s_live[lane] != 0);
       const unsigned mk = __ballot_sync(0xffffffffu, lv);
       if (lv) s_list[__popc(mk & ((1u << lane) - 1u))] = lane;
       if (lane == 0) s_nlive = __popc(mk);
     }
     __syncthreads();
     const int n_live = s_nlive;
-    // ring: slices i .. i + RING - 2 in flight while slice i is summed
+    // ring: slices i .. i + RING - 2 in flight while slice i is summed (the
+    // first chunk's prefetched slices are ring slots 0 .. kPre - 1)
 #pragma unroll
     for (int i = 0; i < Sh::RING - 1; ++i) {
+      if (c0 == 0 && i < kPre) continue;
       if (i < n_live) issue(c0 + s_list[i], i);
       cp_async_commit();
     }
     for (int i = 0; i < n_live; ++i) {
       if (i + Sh::RING - 1 < n_live) issue(c0 + s_list[i + Sh::RING - 1], (i + Sh::RING - 1) % Sh::RING);
       cp_async_commit();
-      cp_async_wait<Sh::RING - 1>();  // this thread's copies of slice i have landed
-      __syncthreads();                 // ... and every thread's
+      cp_async_wait<Sh::RING - 1>();  // this thread's pieces of part i have landed
       const uint4 *slot = reinterpret_cast<const uint4 *>(ring + (i % Sh::RING) * Sh::SLICE);
       const int sc = s_list[i];
 #pragma unroll
       for (int o = 0; o < Sh::OPT; ++o) {
         const int oc = grp * Sh::OPT + o;
-        const uint4 x = slot[oc * kD + dl];
+        const uint4 x = slot[o * 256 + tid];
         const float4 wa = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oc]);
         const float4 wb = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oc + 4]);
         const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
@@ -254,12 +269,12 @@ __global__ void __launch_bounds__(256, SegShape<kD>::CTAS) merge_segment_stream(
           a[8 * o + k] += (w[k] != 0.0f) ? w[k] * e : 0.0f;
         }
       }
-      __syncthreads();  // slot i % RING is refilled by the next iteration
     }
     cp_async_wait<0>();
     __syncthreads();  // s_w / s_live are refilled by the next chunk
   }
-  // [row][dim] through shared memory (the ring is free now), then 16-byte row pieces
+  // [row][dim] through shared memory (the ring is free now: every thread has
+  // passed the barrier after its last part), then 16-byte row pieces
   uint16_t *s_o = reinterpret_cast<uint16_t *>(ring);  // [64][kD + 8]
 #pragma unroll
   for (int o = 0; o < Sh::OPT; ++o)
@@ -463,8 +478,7 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
       set_error("mla_merge_segments: bad row-block count (%lld)", (long long)ctas);
       return MLA_ERR_UNSUPPORTED;
     }
-    // dims per CTA: 128 (two CTAs per SM), or 64 (four) when there are too
-    // few units to give every SM two CTAs
+    // dims per CTA: 128 (two CTAs per SM) or 64 (three)
     int dev = 0, sms = 0;
     cudaError_t e0 = cudaGetDevice(&dev);
     if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -482,7 +496,13 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
       if (e0 != cudaSuccess) return cuda_fail(e0, "cudaFuncSetAttribute(merge smem)");
       g_seg_attr_set[dev].store(true, std::memory_order_relaxed);
     }
-    if (ctas * (512 / 128) >= 2LL * 2 * sms)
+    // the wider slab when its last wave of CTAs is at least as full (fewer
+    // statistics passes per output), else the narrower one
+    auto fill = [&](int64_t tasks, int per_sm) {
+      const int64_t slots = static_cast<int64_t>(per_sm) * sms;
+      return static_cast<double>(tasks) / static_cast<double>(((tasks + slots - 1) / slots) * slots);
+    };
+    if (fill(ctas * 4, SegShape<128>::CTAS) >= fill(ctas * 8, SegShape<64>::CTAS))
       merge_segment_stream<128><<<dim3(static_cast<unsigned>(ctas), 512 / 128), 256, SegShape<128>::DYN, stream>>>(p);
     else
       merge_segment_stream<64><<<dim3(static_cast<unsigned>(ctas), 512 / 64), 256, SegShape<64>::DYN, stream>>>(p);
