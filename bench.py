@@ -582,7 +582,7 @@ class StepBench:
         if "segment_merge" in parts:
             mb = segment_merge_bytes(wl)
             ms = parts["segment_merge"]
-            merges["segment_merge"] = {"kernel": "merge_segment_stream", "bytes": mb, "avg_launch_ms": ms,
+            merges["segment_merge"] = {"kernel": "merge_segment_octets", "bytes": mb, "avg_launch_ms": ms,
                                        "gbs": mb["total"] / (ms * 1e-3) / 1e9,
                                        "frac": mb["total"] / (ms * 1e-3) / 1e9 / hbm}
         if "state_merge" in parts:
@@ -635,7 +635,7 @@ def bandwidth_sized_merge(dev, stream, timer, n, peaks):
     if code:
         raise RuntimeError(f"device error {mla.DEVICE_ERRORS.get(code, code)} in the merge leg")
     gbs = mb["total"] / (ms * 1e-3) / 1e9
-    return {"kernel": "merge_segment_stream", "workload": wl.name + "_uniform_split",
+    return {"kernel": "merge_segment_octets", "workload": wl.name + "_uniform_split",
             "bytes": mb, "avg_launch_ms": ms, "gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
             "l2": f"inputs {mb['total'] / 1e6:.0f} MB > 2 x L2; {per} launches back to back per event bracket"}
 

@@ -15,15 +15,12 @@
 //
 // Segment partials come in the decode kernel's block layout: per (request,
 // 64-row block, segment) a bf16 block [8 row octets][512 dims][8 rows].  One
-// CTA merges 64 output dims of one row block: warp w takes dims 8w..8w+7 of
-// the CTA's 64, lane l the rows of octet l/4 for two of those dims, so every
-// segment costs a warp two 16-byte loads per lane over eight 128-byte runs
-// (the live segments eight at a time), with per-row weights staged in shared memory;
-// the merged 64 x 64 tile is transposed in shared memory and written as
-// 128-byte row pieces.
-// State partials are row-major [W][T*H][512] bf16: one 128-thread block per
-// (row, head), thread t owning dims 4t..4t+3.  Both are HBM/L2 streaming
-// reductions.
+// CTA merges one row octet of one row block: every part's octet is one
+// contiguous 8 KB run, streamed through a per-thread cp.async ring in shared
+// memory (thread t: dims 2t, 2t + 1 of the 8 rows), with each row's
+// statistics read once.  State partials are row-major [W][T*H][512] bf16: one
+// warp per (row, head), lane l owning dims 16l .. 16l + 15.  Both are HBM/L2
+// streaming reductions.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -92,205 +89,148 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Shape of one segment-merge CTA: kD output dims of one unit, 256 threads,
-// live parts streamed through a ring of kRing slices in shared memory.
-template <int kD>
-struct SegShape {
-  static constexpr int G = 256 / kD;             // row groups: thread t takes rows of group t / kD
-  static constexpr int OPT = 8 / G;              // row octets per thread
-  static constexpr int SLICE = 8 * kD * 16;      // bytes of one part's slice (kD dims x 8 octets x 16 B)
-  static constexpr int RING = kD == 128 ? 5 : 6;
-  static constexpr int CTAS = kD == 128 ? 2 : 3;  // per SM
-  static constexpr int DYN = RING * SLICE;       // dynamic shared memory
-};
+constexpr int kOctRing = 8;   // segment merge: parts in the ring (kOctRing - 1 in flight)
+constexpr int kOctCtas = 3;   // segment merge: CTAs per SM
+constexpr int kOctSlot = 8 * 1024;  // one part's octet: [512 dims][8 rows] bf16
+constexpr int kOctDyn = kOctRing * kOctSlot;
 
-// grid (V * B * RB, 512 / kD), 256 threads: one (view, request, row block)
-// unit x kD output dims.  The unit's 64 rows x S statistics are contiguous:
-// one pass gives every row its max and denominator (four threads per row,
-// each a running pair rescaled as its max grows) and keeps the maxima of the
-// first 32 segments in shared memory; the normalised weights 2^(m_s - M) / den
-// of 32 segments at a time are then formed there and the segments with a
-// non-zero weight listed.  Thread t sums dim t % kD for the rows of its row
-// octets: the 16-byte (8-row) pieces of those octets of every live part
-// stream through the thread's own slots of a kRing-deep ring in shared
-// memory with cp.async (a commit group per part, kRing - 1 parts in flight),
-// so a CTA keeps up to (kRing - 1) x 8 x kD x 16 bytes of reads in flight
-// without holding them in registers, and since every thread reads back only
-// the pieces it copied itself, no barrier is needed inside the stream.  A
-// warp's copy covers 32 consecutive dims of one octet, whole 128-byte runs.
-// The merged tile leaves through shared memory as 16-byte row pieces.
-template <int kD>
-__global__ void __launch_bounds__(256, SegShape<kD>::CTAS) merge_segment_stream(const SegParams p) {
-  using Sh = SegShape<kD>;
-  extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(16) float s_m[kSegChunk][kBlockRows];
-  __shared__ __align__(16) float s_w[kSegChunk][kBlockRows];
-  __shared__ float s_part[4][kBlockRows], s_dpart[4][kBlockRows];
+// grid (V * B * RB * 8), 256 threads: one (view, request, row block) unit x
+// one row octet (8 rows).  Warp r takes the statistics of row r of the octet:
+// its lanes the segments (32 at a time), warp reductions give the row's max
+// and denominator; the normalised weights 2^(m_s - M) / den of 32 segments at
+// a time go to shared memory and the segments with a weight for any of the 8
+// rows are listed.  A part's octet is one contiguous 8 KB run of its block
+// ([512 dims][8 rows]); thread t sums dims 2t and 2t + 1 for the 8 rows,
+// streaming its two 16-byte pieces of every listed part through its own
+// places in a kOctRing-deep shared-memory ring with cp.async (a commit group
+// per part, up to kOctRing - 1 parts in flight, no registers held and, since
+// a thread reads back only what it copied, no barrier inside the stream).
+// The first two segments are copied before the statistics are known (a
+// request's first segments hold its tokens; one that turns out empty just
+// gets weight 0, which selects 0), so that their round trip overlaps the
+// statistics'.  Each output row leaves as 128-byte warp stores.
+__global__ void __launch_bounds__(256, kOctCtas) merge_segment_octets(const SegParams p) {
+  extern __shared__ __align__(128) uint8_t ring[];  // [kOctRing][256 threads][2] x 16 B
+  __shared__ __align__(16) float s_w[kSegChunk][8];
+  __shared__ float s_M[8], s_inv[8];
   __shared__ int s_live[kSegChunk], s_list[kSegChunk], s_nlive;
-  __shared__ float s_M[kBlockRows], s_inv[kBlockRows];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // block (view, request, row block): vb = v * B + b
-  const int vb = blockIdx.x / p.row_blocks, rb = blockIdx.x % p.row_blocks;
+  const int unit = blockIdx.x >> 3, oct = blockIdx.x & 7;
+  // unit (view, request, row block): vb = v * B + b
+  const int vb = unit / p.row_blocks, rb = unit % p.row_blocks;
   const int v = vb / p.num_reqs, b = vb % p.num_reqs;
   const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
   if (q0 < 0 || q1 < q0 || q1 > p.num_rows) return;  // flagged by the decode kernel
   const int rows_req = (q1 - q0) * p.num_heads;
-  const int n_rows = min(kBlockRows, rows_req - rb * kBlockRows);
+  const int n_rows = min(8, rows_req - rb * kBlockRows - 8 * oct);  // rows of this octet
   if (n_rows <= 0) return;
   const int S = p.num_parts;
-  const int64_t grow0 = (static_cast<int64_t>(v) * p.num_rows + q0) * p.num_heads + rb * kBlockRows;  // first row
-  const float *mx = p.segm_max + grow0 * S;  // [64 rows][S], contiguous
+  const int64_t grow0 = (static_cast<int64_t>(v) * p.num_rows + q0) * p.num_heads + rb * kBlockRows + 8 * oct;
+  const float *mx = p.segm_max + grow0 * S;  // [8 rows][S], contiguous
   const float *sm = p.segm_sum + grow0 * S;
-  const int dim0 = blockIdx.y * kD;
-
-  const int dl = tid % kD, grp = tid / kD;
-  float a[Sh::OPT * 8];  // rows 8 (grp * OPT + o) + k
-#pragma unroll
-  for (int k = 0; k < Sh::OPT * 8; ++k) a[k] = 0.0f;
   const int64_t blk0 = (static_cast<int64_t>(vb) * p.row_blocks + rb) * S;
   const uint32_t s_ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-  // this thread's pieces of part `sc` into its own places in ring slot `slot`:
-  // slot [256 threads][OPT] x 16 B
+  // this thread's pieces (dims 2 tid and 2 tid + 1, 8 rows each) of part `sc` into ring slot `slot`
   auto issue = [&](int sc, int slot) {
-    const uint4 *blk = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + sc) * (512 * kBlockRows));
-#pragma unroll
-    for (int o = 0; o < Sh::OPT; ++o)
-      cp_async16(s_ring + slot * Sh::SLICE + (o * 256 + tid) * 16, blk + (grp * Sh::OPT + o) * 512 + dim0 + dl);
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.segm_out + (blk0 + sc) * (512 * kBlockRows)) + oct * 512 + 2 * tid;
+    const uint32_t dst = s_ring + slot * kOctSlot + tid * 32;
+    cp_async16(dst, src);
+    cp_async16(dst + 16, src + 1);
   };
-  // The first two segment slots are copied before the statistics are known
-  // (a request's first slots hold its tokens; a slot that turns out empty
-  // just gets weight 0, which selects 0), so that the statistics' round trip
-  // overlaps the first data copies; the ring's other slots start after it.
   constexpr int kPre = 2;
-  static_assert(kPre <= Sh::RING - 1, "prefetched slots fit the ring");
   const int n_pre = min(kPre, S);
 #pragma unroll
-  for (int i = 0; i < Sh::RING - 1; ++i) {
+  for (int i = 0; i < kPre; ++i) {
     if (i < n_pre) issue(i, i);
-    if (i < kPre) cp_async_commit();
+    cp_async_commit();
   }
-  const int row = tid & (kBlockRows - 1), quarter = tid >> 6;
-  float Mq = -INFINITY, dq = 0.0f;
-  auto take = [&](float m, float l) {
-    if (m == -INFINITY) return;
-    if (m > Mq) {
-      dq = dq * exp2f(Mq - m) + l;  // 0 while Mq is -inf
-      Mq = m;
-    } else {
-      dq += exp2f(m - Mq) * l;
-    }
-  };
+  // row statistics: warp r, lanes over the segments, a running (max, sum)
   {
-    float mv[8], lv[8];  // the first 32 segments, loaded at once
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int s2 = quarter + 4 * j;
-      const bool in = row < n_rows && s2 < S;
-      mv[j] = in ? mx[row * S + s2] : -INFINITY;
-      lv[j] = in ? sm[row * S + s2] : 0.0f;
+    float M = -INFINITY, d = 0.0f;
+    if (warp < n_rows) {
+      for (int s0 = 0; s0 < S; s0 += 32) {
+        const int s2 = s0 + lane;
+        const float m = s2 < S ? mx[warp * S + s2] : -INFINITY;
+        const float l = s2 < S ? sm[warp * S + s2] : 0.0f;
+        const float nM = fmaxf(M, warp_max(m));
+        if (nM != -INFINITY) {
+          const float part = warp_sum(m != -INFINITY ? exp2f(m - nM) * l : 0.0f);
+          d = (M != -INFINITY ? d * exp2f(M - nM) : 0.0f) + part;
+          M = nM;
+        }
+      }
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      take(mv[j], lv[j]);
-      s_m[quarter + 4 * j][row] = mv[j];
+    if (lane == 0) {
+      s_M[warp] = M;
+      s_inv[warp] = d > 0.0f ? 1.0f / d : 0.0f;
+      if (warp < n_rows) p.lse[grow0 + warp] = d > 0.0f ? (M + log2f(d)) * kLn2 : -INFINITY;
     }
-  }
-  if (row < n_rows)
-    for (int s2 = quarter + 4 * 8; s2 < S; s2 += 4) take(mx[row * S + s2], sm[row * S + s2]);
-  s_part[quarter][row] = Mq;
-  s_dpart[quarter][row] = dq;
-  __syncthreads();
-  if (quarter == 0) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) M = fmaxf(M, s_part[k][row]);
-    float d = 0.0f;
-    if (M != -INFINITY)
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (s_part[k][row] != -INFINITY) d += exp2f(s_part[k][row] - M) * s_dpart[k][row];
-    s_M[row] = M;
-    s_inv[row] = d > 0.0f ? 1.0f / d : 0.0f;
-    if (blockIdx.y == 0 && row < n_rows)
-      p.lse[grow0 + row] = d > 0.0f ? (M + log2f(d)) * kLn2 : -INFINITY;
   }
   __syncthreads();
 
+  float a[16];  // a[2 r]: row r, dim 2 tid;  a[2 r + 1]: row r, dim 2 tid + 1
+#pragma unroll
+  for (int k = 0; k < 16; ++k) a[k] = 0.0f;
   for (int c0 = 0; c0 < S; c0 += kSegChunk) {
     const int nc = min(kSegChunk, S - c0);
-    // normalised weights of this chunk (0 for empty rows / segments / padding rows)
-    if (tid < kSegChunk) s_live[tid] = 0;
+    const int pre = c0 == 0 ? n_pre : 0;  // slots already in the ring, live or not
+    if (tid < kSegChunk) s_live[tid] = tid < pre ? 1 : 0;
     __syncthreads();
-    for (int i = tid; i < nc * kBlockRows; i += 256) {
-      const int sc = i / kBlockRows, rr = i % kBlockRows;
+    {  // weights of this chunk: thread (slot tid / 8, row tid % 8)
+      const int sc = tid >> 3, r = tid & 7;
       float w = 0.0f;
-      if (rr < n_rows && s_M[rr] != -INFINITY) {
-        const float m = c0 == 0 ? s_m[sc][rr] : mx[rr * S + c0 + sc];
-        if (m != -INFINITY) w = exp2f(m - s_M[rr]) * s_inv[rr];
+      if (sc < nc && r < n_rows && s_M[r] != -INFINITY) {
+        const float m = mx[r * S + c0 + sc];
+        if (m != -INFINITY) w = exp2f(m - s_M[r]) * s_inv[r];
       }
-      s_w[sc][rr] = w;
+      s_w[sc][r] = w;
       if (w != 0.0f) s_live[sc] = 1;
     }
     __syncthreads();
-    const int pre = c0 == 0 ? n_pre : 0;  // slots already in the ring, live or not
-    if (warp == 0) {  // the slots to sum, in order: the prefetched ones, then the other live ones
-      const bool lv = lane < nc && (lane < pre || s_live[lane] != 0);
+    if (warp == 0) {  // the slots to sum, in order: the prefetched ones, then the live ones
+      const bool lv = lane < nc && s_live[lane] != 0;
       const unsigned mk = __ballot_sync(0xffffffffu, lv);
       if (lv) s_list[__popc(mk & ((1u << lane) - 1u))] = lane;
       if (lane == 0) s_nlive = __popc(mk);
     }
     __syncthreads();
     const int n_live = s_nlive;
-    // ring: slices i .. i + RING - 2 in flight while slice i is summed (the
-    // first chunk's prefetched slices are ring slots 0 .. kPre - 1)
+    // ring: parts i .. i + kOctRing - 2 in flight while part i is summed (the
+    // first chunk's prefetched parts are ring slots 0 .. kPre - 1)
 #pragma unroll
-    for (int i = 0; i < Sh::RING - 1; ++i) {
+    for (int i = 0; i < kOctRing - 1; ++i) {
       if (c0 == 0 && i < kPre) continue;
       if (i < n_live) issue(c0 + s_list[i], i);
       cp_async_commit();
     }
     for (int i = 0; i < n_live; ++i) {
-      if (i + Sh::RING - 1 < n_live) issue(c0 + s_list[i + Sh::RING - 1], (i + Sh::RING - 1) % Sh::RING);
+      if (i + kOctRing - 1 < n_live) issue(c0 + s_list[i + kOctRing - 1], (i + kOctRing - 1) % kOctRing);
       cp_async_commit();
-      cp_async_wait<Sh::RING - 1>();  // this thread's pieces of part i have landed
-      const uint4 *slot = reinterpret_cast<const uint4 *>(ring + (i % Sh::RING) * Sh::SLICE);
+      cp_async_wait<kOctRing - 1>();  // this thread's pieces of part i have landed
+      const uint4 *slot = reinterpret_cast<const uint4 *>(ring + (i % kOctRing) * kOctSlot) + 2 * tid;
+      const uint4 x0 = slot[0], x1 = slot[1];
       const int sc = s_list[i];
+      const float4 wa = *reinterpret_cast<const float4 *>(&s_w[sc][0]);
+      const float4 wb = *reinterpret_cast<const float4 *>(&s_w[sc][4]);
+      const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      const uint32_t u0[4] = {x0.x, x0.y, x0.z, x0.w};  // dim 2 tid, rows 0..7
+      const uint32_t u1[4] = {x1.x, x1.y, x1.z, x1.w};  // dim 2 tid + 1
 #pragma unroll
-      for (int o = 0; o < Sh::OPT; ++o) {
-        const int oc = grp * Sh::OPT + o;
-        const uint4 x = slot[o * 256 + tid];
-        const float4 wa = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oc]);
-        const float4 wb = *reinterpret_cast<const float4 *>(&s_w[sc][8 * oc + 4]);
-        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-        const uint32_t vv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {  // a weight of 0 selects 0: an empty row's slot is never a value
-          const float e = (k & 1) ? bf16_hi(vv[k >> 1]) : bf16_lo(vv[k >> 1]);
-          a[8 * o + k] += (w[k] != 0.0f) ? w[k] * e : 0.0f;
-        }
+      for (int r = 0; r < 8; ++r) {  // a weight of 0 selects 0: an empty row's slot is never a value
+        const float e0 = (r & 1) ? bf16_hi(u0[r >> 1]) : bf16_lo(u0[r >> 1]);
+        const float e1 = (r & 1) ? bf16_hi(u1[r >> 1]) : bf16_lo(u1[r >> 1]);
+        a[2 * r] += (w[r] != 0.0f) ? w[r] * e0 : 0.0f;
+        a[2 * r + 1] += (w[r] != 0.0f) ? w[r] * e1 : 0.0f;
       }
     }
     cp_async_wait<0>();
-    __syncthreads();  // s_w / s_live are refilled by the next chunk
+    __syncthreads();  // s_w / s_live / s_list are refilled by the next chunk
   }
-  // [row][dim] through shared memory (the ring is free now: every thread has
-  // passed the barrier after its last part), then 16-byte row pieces
-  uint16_t *s_o = reinterpret_cast<uint16_t *>(ring);  // [64][kD + 8]
+  // row r: dims 2 tid, 2 tid + 1 as one 4-byte store; a warp covers 128 bytes of the row
 #pragma unroll
-  for (int o = 0; o < Sh::OPT; ++o)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const __nv_bfloat16 hv = __float2bfloat16_rn(a[8 * o + k]);
-      s_o[(8 * (grp * Sh::OPT + o) + k) * (kD + 8) + dl] = *reinterpret_cast<const uint16_t *>(&hv);
-    }
-  __syncthreads();
-  for (int i = tid; i < kBlockRows * kD / 8; i += 256) {
-    const int r = i / (kD / 8), c16 = i % (kD / 8);
-    if (r < n_rows) {
-      const uint4 val = *reinterpret_cast<const uint4 *>(&s_o[r * (kD + 8) + 8 * c16]);
-      *reinterpret_cast<uint4 *>(p.out + (grow0 + r) * 512 + dim0 + 8 * c16) = val;
-    }
-  }
+  for (int r = 0; r < 8; ++r)
+    if (r < n_rows)
+      reinterpret_cast<uint32_t *>(p.out + (grow0 + r) * 512)[tid] = pack_bf16(a[2 * r], a[2 * r + 1]);
 }
 
 // ---------------------------------------------------------------- states
@@ -452,7 +392,7 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_states(const StateParam
   if (tid == 0) p.lse[it] = M + logf(den);
 }
 
-// Per device: the streaming merges' shared-memory attributes are set (relaxed
+// Per device: the segment merge's shared-memory attribute is set (relaxed
 // atomics: concurrent first calls store the same value).
 std::atomic<bool> g_seg_attr_set[64];
 
@@ -478,34 +418,23 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
       set_error("mla_merge_segments: bad row-block count (%lld)", (long long)ctas);
       return MLA_ERR_UNSUPPORTED;
     }
-    // dims per CTA: 128 (two CTAs per SM) or 64 (three)
-    int dev = 0, sms = 0;
+    int dev = 0;
     cudaError_t e0 = cudaGetDevice(&dev);
-    if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e0 != cudaSuccess) return cuda_fail(e0, "merge: SM count");
+    if (e0 != cudaSuccess) return cuda_fail(e0, "merge: device");
     if (dev < 0 || dev >= 64) {
       set_error("device ordinal %d out of range", dev);
       return MLA_ERR_CUDA;
     }
     if (!g_seg_attr_set[dev].load(std::memory_order_relaxed)) {
-      e0 = cudaFuncSetAttribute(merge_segment_stream<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SegShape<128>::DYN);
-      if (e0 == cudaSuccess)
-        e0 = cudaFuncSetAttribute(merge_segment_stream<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  SegShape<64>::DYN);
+      e0 = cudaFuncSetAttribute(merge_segment_octets, cudaFuncAttributeMaxDynamicSharedMemorySize, kOctDyn);
       if (e0 != cudaSuccess) return cuda_fail(e0, "cudaFuncSetAttribute(merge smem)");
       g_seg_attr_set[dev].store(true, std::memory_order_relaxed);
     }
-    // the wider slab when its last wave of CTAs is at least as full (fewer
-    // statistics passes per output), else the narrower one
-    auto fill = [&](int64_t tasks, int per_sm) {
-      const int64_t slots = static_cast<int64_t>(per_sm) * sms;
-      return static_cast<double>(tasks) / static_cast<double>(((tasks + slots - 1) / slots) * slots);
-    };
-    if (fill(ctas * 4, SegShape<128>::CTAS) >= fill(ctas * 8, SegShape<64>::CTAS))
-      merge_segment_stream<128><<<dim3(static_cast<unsigned>(ctas), 512 / 128), 256, SegShape<128>::DYN, stream>>>(p);
-    else
-      merge_segment_stream<64><<<dim3(static_cast<unsigned>(ctas), 512 / 64), 256, SegShape<64>::DYN, stream>>>(p);
+    if (ctas * 8 > INT32_MAX) {
+      set_error("mla_merge_segments: too many row blocks (%lld)", (long long)ctas);
+      return MLA_ERR_UNSUPPORTED;
+    }
+    merge_segment_octets<<<static_cast<unsigned>(ctas * 8), 256, kOctDyn, stream>>>(p);
   } else {
     StateParams p{};
     p.part_out = static_cast<const __nv_bfloat16 *>(m.part_out);
