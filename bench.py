@@ -44,7 +44,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode/verify KV-read GB/s (% of GB300 HBM peak) and query-rows/sec"
 L2_FLUSH_BYTES = 256 << 20
-WORKLOADS = ["dcp8", "verify_mtp4", "fp8_mixed", "decode_qlen1"]
+WORKLOADS = ["dcp8", "verify_mtp4", "fp8_mixed", "decode_qlen1", "wide_rows"]
 
 
 def parse():
@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dcp8", choices=WORKLOADS)
-    ap.add_argument("--extra", default="verify_mtp4,fp8_mixed",
+    ap.add_argument("--extra", default="verify_mtp4,fp8_mixed,wide_rows",
                     help="comma-separated workloads also timed into the line ('none': skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -73,6 +73,13 @@ def make_workload(name, seed, device=None):
         return workloads.fp8_mixed_qlen(seed=seed, device=device)
     if name == "dcp8":
         return workloads.dcp8_verify_bf16(seed=seed, device=device)
+    if name == "wide_rows":
+        # the sweep's widest rows: 128 heads x qlen 8 (16 64-row blocks per
+        # request), seq_len U{6k..12k}, bf16, block 64, 8 split-K slots
+        g = np.random.default_rng(seed + 911)
+        L = g.integers(6000, 12001, 6)
+        return workloads.make_workload("wide_rows_bf16_b6_h128_qlen8_L6k-12k_bs64_s8", L, [8] * 6, 128, 64,
+                                       "bf16", 1, 8, seed, device=device)
     return workloads.decode_qlen1_bf16(seed=seed)
 
 
@@ -168,6 +175,19 @@ def split_parts(wl, grid=None, uniform=False):
                 for t in range(ql):
                     active += -(-_local(L - ql + 1 + t, r, W, I) // seg_tok) * H
     return active, S, balanced
+
+
+def algorithmic_flops(wl) -> int:
+    """2 * sum over (view, row, head) of the row's visible tokens * (576 + 512):
+    the QK^T and PV multiply-adds of the exact causal windows (unpadded heads,
+    masked keys excluded)."""
+    W, I, H = wl.world_size, wl.interleave, wl.num_heads
+    tot = 0
+    for r in range(W):
+        for b in range(wl.num_reqs):
+            L, ql = int(wl.seq_lens[b]), int(wl.qlens[b])
+            tot += sum(_local(L - ql + 1 + t, r, W, I) for t in range(ql))
+    return 2 * H * tot * (576 + 512)
 
 
 def decode_unit_bytes(wl, grid=None, uniform=False) -> dict:
@@ -572,12 +592,25 @@ class StepBench:
             dms = parts["decode"]
             kname = "mla_decode_kernel<bf16>" if wl.kv_dtype == "bf16" else "mla_decode_kernel<fp8>"
             achieved = ub["total"] / (dms * 1e-3) / 1e9
-            res["roofline"] = {
-                "kernel": kname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
-                "traffic": recorded_traffic(kname, wl.name), "algorithmic_bytes": ub,
-                "avg_launch_ms": dms, "kv_only_gbs": ub["kv"] / (dms * 1e-3) / 1e9,
-                "kv_only_frac": ub["kv"] / (dms * 1e-3) / 1e9 / hbm}
+            fl = algorithmic_flops(wl)
+            ridge = peaks["bf16_tflops"] * 1e12 / (hbm * 1e9)  # FLOP per byte where the roofs meet
+            if fl / ub["kv"] > ridge:
+                # heads x qlen rows against one KV tile: a dense bf16 contraction
+                tf = fl / (dms * 1e-3) / 1e12
+                res["roofline"] = {
+                    "kernel": kname, "bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                    "peak_source": f"{peak_kind} bf16_tflops (cuBLAS, burst)", "traffic": None,
+                    "algorithmic_flops": fl, "intensity_flop_per_kv_byte": fl / ub["kv"],
+                    "ridge_flop_per_byte": ridge, "avg_launch_ms": dms,
+                    "kv_only_gbs": ub["kv"] / (dms * 1e-3) / 1e9, "algorithmic_bytes": ub}
+            else:
+                res["roofline"] = {
+                    "kernel": kname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved / hbm, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                    "traffic": recorded_traffic(kname, wl.name), "algorithmic_bytes": ub,
+                    "avg_launch_ms": dms, "kv_only_gbs": ub["kv"] / (dms * 1e-3) / 1e9,
+                    "kv_only_frac": ub["kv"] / (dms * 1e-3) / 1e9 / hbm}
         merges = {}
         if "segment_merge" in parts:
             mb = segment_merge_bytes(wl)
