@@ -94,6 +94,8 @@ struct TableArgs {
 __global__ void plan_kernel(int B, int T, const int32_t *seq_lens, const int32_t *ind,
                             int32_t *row_len, int32_t *row_req, TableArgs tab, int row_blocks,
                             int *err) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int total = ind[B];
   const bool ind_ok = ind[0] == 0 && total >= 0 && total <= T;
   if (blockIdx.x >= row_blocks) {
@@ -136,6 +138,8 @@ __global__ void plan_kernel(int B, int T, const int32_t *seq_lens, const int32_t
 __global__ void shard_kernel(int B, int T, const int32_t *ind, const int32_t *row_len_global,
                              int W, int rank0, int I, int32_t *row_len_local, TableArgs tab,
                              int row_blocks, int *err, int64_t bt_view_stride, int64_t sp_view_stride) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int rank = rank0 + static_cast<int>(blockIdx.y);
   row_len_local += static_cast<int64_t>(blockIdx.y) * T;
   if (tab.bt != nullptr) {
@@ -276,8 +280,8 @@ mla_status launch_plan_rows(int B, int T, const int32_t *seq_lens, const int32_t
   TableArgs tab{t.block_table, t.bt_stride, t.num_blocks, t.block_size, t.page_size,
                 t.subpage_table, t.sp_stride};
   const int blocks = row_blocks + (t.block_table != nullptr ? B : 0);
-  plan_kernel<<<blocks, 256, 0, stream>>>(B, T, seq_lens, ind, row_len, row_req, tab, row_blocks, err);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(plan_kernel, dim3(blocks), dim3(256), 0, stream, B, T, seq_lens, ind, row_len,
+                                   row_req, tab, row_blocks, err);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan_rows launch");
 }
 
@@ -289,9 +293,9 @@ mla_status launch_shard_rows(int B, int T, const int32_t *ind, const int32_t *ro
                 t.subpage_table, t.sp_stride};
   const int blocks = row_blocks + (t.block_table != nullptr ? B : 0);
   const int64_t bt_view = static_cast<int64_t>(B) * t.bt_stride, sp_view = static_cast<int64_t>(B) * t.sp_stride;
-  shard_kernel<<<dim3(blocks, num_views), 256, 0, stream>>>(B, T, ind, row_len_global, W, rank, interleave,
-                                                            row_len_local, tab, row_blocks, err, bt_view, sp_view);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(shard_kernel, dim3(blocks, num_views), dim3(256), 0, stream, B, T, ind,
+                                   row_len_global, W, rank, interleave, row_len_local, tab, row_blocks, err,
+                                   bt_view, sp_view);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "shard_row_view launch");
 }
 

@@ -656,6 +656,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc.n_pend = 0;
     fence_mbar_init();
   }
+  // Nothing above touched global memory: the previous kernel in the stream
+  // (which may produce this call's inputs, or read what it overwrites) has
+  // completed from here on.
+  grid_dep_wait();
+  grid_dep_launch();
   const bool balanced = p.balanced != 0;
   // Balanced split: the producer's one chunk.  With the merge in this kernel
   // it is claimed from the work counter (a holder waits only for chunks that
@@ -1636,10 +1641,14 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream, bool *merge
   p.out_scale = kv_scale;
 
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-  e = cudaMemsetAsync(d.sched, 0, d.state_bytes, stream);  // work counter + unit counters
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(work counters)");
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
-  e = cudaGetLastError();
+  // The work counter and the unit counters are read only by the dynamic
+  // schedule and by the in-kernel merge; the balanced split alone takes
+  // chunk c on CTA c and needs neither.
+  if (!p.balanced || p.fused) {
+    e = cudaMemsetAsync(d.sched, 0, d.state_bytes, stream);  // work counter + unit counters
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(work counters)");
+  }
+  e = launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, tm_q, tm_kv, p);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return MLA_OK;
 }

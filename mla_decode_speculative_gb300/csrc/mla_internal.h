@@ -29,6 +29,34 @@ mla_status make_tmap_tile3d(CUtensorMap *map, const void *base, CUtensorMapDataT
                             int elem_bytes, uint64_t rows, uint32_t box_rows,
                             CUtensorMapSwizzle swizzle);
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization: its CTAs may be scheduled while the
+// kernel before it in the stream is still finishing, run their prologue
+// (barriers, tensor memory), and then block in grid_dep_wait() until that
+// kernel has completed and its memory is visible -- before their first
+// global-memory access, read or write.  grid_dep_launch() lets the next
+// kernel's CTAs be scheduled (they still wait for this grid to complete).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Launchers (arguments already validated on the host).
 struct TableLaunch {  // optional sub-page expansion (block_table == nullptr: none)
   const int32_t *block_table;

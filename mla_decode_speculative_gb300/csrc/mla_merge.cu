@@ -110,6 +110,8 @@ constexpr int kOctDyn = kOctRing * kOctSlot;
 // gets weight 0, which selects 0), so that their round trip overlaps the
 // statistics'.  Each output row leaves as 128-byte warp stores.
 __global__ void __launch_bounds__(256, kOctCtas) merge_segment_octets(const SegParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ __align__(128) uint8_t ring[];  // [kOctRing][256 threads][2] x 16 B
   __shared__ __align__(16) float s_w[kSegChunk][8];
   __shared__ float s_M[8], s_inv[8];
@@ -244,6 +246,8 @@ constexpr int kStateBatch = 8;  // parts read at a time
 // shards); a part with lse = -inf gets weight 0, which selects 0, so its row
 // is never used as a value.
 __global__ void __launch_bounds__(kStateWarps * 32) merge_states_small(const StateParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const int64_t it = static_cast<int64_t>(blockIdx.x) * kStateWarps + (threadIdx.x >> 5);
   if (it >= p.num_items) return;
@@ -313,6 +317,8 @@ __device__ __forceinline__ float4 load_state4(const StateParams &p, int64_t it, 
 // Any number of parts: live parts are compacted, in order, into shared
 // memory, then streamed with eight loads in flight per thread.
 __global__ void __launch_bounds__(kThreadsPerItem) merge_states(const StateParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ float s_w[kMaxParts];
   __shared__ int s_idx[kMaxParts];
   __shared__ float s_red[kThreadsPerItem / 32];
@@ -434,7 +440,9 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
       set_error("mla_merge_segments: too many row blocks (%lld)", (long long)ctas);
       return MLA_ERR_UNSUPPORTED;
     }
-    merge_segment_octets<<<static_cast<unsigned>(ctas * 8), 256, kOctDyn, stream>>>(p);
+    const cudaError_t el = launch_pdl(merge_segment_octets, dim3(static_cast<unsigned>(ctas * 8)), dim3(256), kOctDyn,
+                                      stream, p);
+    if (el != cudaSuccess) return cuda_fail(el, "merge launch");
   } else {
     StateParams p{};
     p.part_out = static_cast<const __nv_bfloat16 *>(m.part_out);
@@ -451,9 +459,11 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
     const unsigned blocks = static_cast<unsigned>(p.num_items);
     if (p.num_parts <= 32) {
       const unsigned ctas = static_cast<unsigned>((p.num_items + kStateWarps - 1) / kStateWarps);
-      merge_states_small<<<ctas, kStateWarps * 32, 0, stream>>>(p);
+      const cudaError_t el = launch_pdl(merge_states_small, dim3(ctas), dim3(kStateWarps * 32), 0, stream, p);
+      if (el != cudaSuccess) return cuda_fail(el, "merge launch");
     } else {
-      merge_states<<<blocks, kThreadsPerItem, 0, stream>>>(p);
+      const cudaError_t el = launch_pdl(merge_states, dim3(blocks), dim3(kThreadsPerItem), 0, stream, p);
+      if (el != cudaSuccess) return cuda_fail(el, "merge launch");
     }
   }
   const cudaError_t e = cudaGetLastError();
