@@ -92,24 +92,27 @@ def kv_bytes(wl) -> int:
 
 def _balanced_parts(unit_tiles, S, grid):
     """Tile ranges of the balanced split's parts, per unit (the default split of
-    mla_decode_verify as its header states it): the units' T tiles end to end,
-    n = min(grid, T // ceil(tmax / (S-1))) chunks [floor(cT/n), floor((c+1)T/n));
+    mla_decode_verify as its header states it): each unit with t > 0 tiles is
+    one overhead position then its t tiles, V positions end to end,
+    n = min(grid, V // ceil(tmax / (S-1))) chunks [floor(cV/n), floor((c+1)V/n));
     a unit's part in chunk c is one segment."""
-    T, tmax = int(sum(unit_tiles)), int(max(unit_tiles))
+    V = int(sum(int(t) + 1 for t in unit_tiles if int(t) > 0))
+    tmax = int(max(unit_tiles))
     need = max(-(-tmax // (S - 1)), 1)
-    n = min(grid, max(T // need, 1)) if T else 1
-    bounds = [c * T // n for c in range(n + 1)]
-    parts, start = [], 0
+    n = min(grid, max(V // need, 1)) if V else 1
+    bounds = [c * V // n for c in range(n + 1)]
+    parts, pos = [], 0
     for t in unit_tiles:
         t = int(t)
         lst = []
         if t:
+            start = pos + 1  # past the overhead position
             c = next(c for c in range(n) if bounds[c + 1] > start)
             while c < n and bounds[c] < start + t:
                 lst.append((max(bounds[c], start) - start, min(bounds[c + 1], start + t) - start))
                 c += 1
+            pos = start + t
         parts.append(lst)
-        start += t
     return parts
 
 
@@ -129,7 +132,7 @@ def is_balanced(wl, uniform=False):
     RB = -(-int(max(wl.qlens)) * H // 64)
     max_len = max(1, -(-int(wl.max_kv_len) // P)) * P  # the static bound the step passes
     return (not uniform and S > 1 and W * B * RB <= 1024
-            and W * B * RB * -(-max_len // 64) <= 2 ** 31 - 1)
+            and W * B * RB * (-(-max_len // 64) + 1) <= 2 ** 31 - 1)
 
 
 def balanced_units(wl, grid=None):

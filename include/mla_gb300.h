@@ -206,13 +206,15 @@ typedef enum mla_decode_flags {
   MLA_DECODE_SKIP_MERGE = 1,
   /* How the S > 1 segment slots are filled.  Default (flag clear, at most
    * 1024 (view, request, row block) units, and units x the static bound's
-   * tiles (subpage_stride * P / 64) within int32): balanced split -- the units'
-   * 64-token KV tiles, laid end to end in unit order, are cut into equal
-   * contiguous chunks, one per SM (grown where needed so that no unit meets
-   * more than S chunks); the part of a unit inside chunk c is its segment
-   * c - c0 (c0: the unit's first chunk), and slots past a unit's last part
-   * hold max = -inf, sum = 0.  Every SM then streams the same number of
-   * tiles, whatever the mix of lengths.  With this flag (or beyond those
+   * tiles plus one (subpage_stride * P / 64 + 1) within int32): balanced
+   * split -- every unit with tiles counts as one overhead position (its Q load
+   * and epilogue cost about one tile) followed by its 64-token KV tiles; the
+   * positions of all units, laid end to end in unit order, are cut into
+   * equal contiguous chunks, one per SM (grown where needed so that no unit
+   * meets more than S chunks); the part of a unit inside chunk c is its
+   * segment c - c0 (c0: the first chunk holding one of its tiles), and slots
+   * past a unit's last part hold max = -inf, sum = 0.  Every SM then does
+   * the same work, whatever the mix of lengths.  With this flag (or beyond those
    * bounds): the pages' split [vLLM #51705, 实现拆解 4] -- segment s of a request holds
    * tokens [s*L, (s+1)*L) with L = ceil(len / (S*P)) * P, len the
    * request's longest visible row.  The merged out / lse are the same either

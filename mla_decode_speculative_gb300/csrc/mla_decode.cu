@@ -128,7 +128,7 @@ struct Misc {
   int sm_stop[2];  // softmax warps' shared exit decision (double-buffered)
   int req_key[kMaxOrderedReqs];   // a request's longest row (producer's scratch)
   int req_order[kMaxOrderedReqs]; // requests, longest first
-  int unit_end[kMaxUnits];        // balanced split: tiles of units 0..u (inclusive prefix sum)
+  int unit_end[kMaxUnits];        // balanced split: tiles of unit u, then positions of units 0..u (prefix sum)
   float red[2][2][4][32];  // [buffer][column group][lane quarter][lane]
   PendMerge pend[kMaxPend];       // softmax warps: merges to run after the CTA's own parts
   int n_pend;
@@ -740,19 +740,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       order = misc.req_order;
     }
-    // Balanced split: the units' T tiles laid end to end are cut into n
-    // chunks, chunk c = [floor(c T / n), floor((c+1) T / n)), one per CTA
-    // (n smaller when that keeps every unit within S chunks); a chunk's part
-    // of each unit it meets is one segment of that unit, numbered by chunk
-    // from the unit's first.
+    // Balanced split: every unit with tiles is one overhead position (the
+    // part's Q load and epilogue cost about one tile) followed by its tiles;
+    // the V positions of all units laid end to end are cut into n chunks,
+    // chunk c = [floor(c V / n), floor((c+1) V / n)), one per CTA (n smaller
+    // when that keeps every unit within S chunks); a chunk's part of each
+    // unit whose tiles it meets is one segment of that unit, numbered by
+    // chunk from the unit's first.
     const int n_units = p.num_units;
-    int T = 0, n_chunks = 0;
+    int T = 0, n_chunks = 0;  // T: V, the positions (tiles + overheads)
     if (balanced) {
       int carry = 0, tmax = 0;
       for (int base = 0; base < n_units; base += 32) {  // inclusive prefix sum, in place
         const int u = base + lane;
-        int x = u < n_units ? misc.unit_end[u] : 0;
-        tmax = max(tmax, x);
+        const int t = u < n_units ? misc.unit_end[u] : 0;
+        tmax = max(tmax, t);
+        int x = t > 0 ? t + 1 : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -769,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int need = max((tmax + S - 2) / (S - 1), 1);
       n_chunks = T > 0 ? min(static_cast<int>(gridDim.x), max(T / need, 1)) : 1;
     }
-    // chunk holding tile x (T > 0)
+    // chunk holding position x (T > 0)
     auto chunk_of = [&](int x) {
       return static_cast<int>((static_cast<long long>(x + 1) * n_chunks - 1) / T);
     };
@@ -819,7 +822,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           while (u_next < n_units) {
             const int u = u_next;
             const int end = misc.unit_end[u];
-            const int start = u == 0 ? 0 : misc.unit_end[u - 1];
+            const int prev = u == 0 ? 0 : misc.unit_end[u - 1];
+            const int start = prev + (end > prev ? 1 : 0);  // first tile, past the overhead position
             if (start >= c_hi_ext) break;
             ++u_next;
             if (end > start && end <= c_lo) continue;  // all of its tiles lie before this chunk
@@ -1622,10 +1626,11 @@ mla_status launch_decode(const DecodeLaunch &d, cudaStream_t stream, bool *merge
   p.tile3d = tile3d ? 1 : 0;
   const int64_t units = static_cast<int64_t>(a.num_reqs) * V * p.row_blocks;
   p.num_units = static_cast<int>(units);
-  // the balanced split counts tiles in int32: every unit at the static bound must fit
+  // the balanced split counts positions (tiles + one per unit) in int32:
+  // every unit at the static bound must fit
   const int64_t max_unit_tiles = (static_cast<int64_t>(a.subpage_stride) * a.page_size + kTileTok - 1) / kTileTok;
   p.balanced = (a.num_segments >= 2 && (a.flags & MLA_DECODE_UNIFORM_SEGMENTS) == 0 && units <= kMaxUnits &&
-                units * max_unit_tiles <= INT32_MAX)
+                units * (max_unit_tiles + 1) <= INT32_MAX)
                    ? 1
                    : 0;
   p.unit_state = d.unit_state;

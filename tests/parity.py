@@ -120,18 +120,22 @@ def blocks_to_rows(blocks, qo_indptr, num_heads, num_rows):
 
 
 def balanced_parts(unit_tiles, S, grid):
-    """The balanced split as the header states it, restated for the test: the
-    units' T tiles end to end, n chunks [floor(cT/n), floor((c+1)T/n)) with
-    n = min(grid, T // need), need = ceil(tmax / (S-1)) (so no unit meets more
-    than S chunks); unit u's part in chunk c is its segment c - (chunk of its
-    first tile).  Returns {u: [(tile_lo, tile_hi) per segment]}."""
-    T, tmax = sum(unit_tiles), max(unit_tiles)
+    """The balanced split as the header states it, restated for the test: a
+    unit with t > 0 tiles is one overhead position followed by its t tiles;
+    the V positions end to end are cut into n chunks [floor(cV/n),
+    floor((c+1)V/n)) with n = min(grid, V // need), need = ceil(tmax / (S-1))
+    (so no unit meets more than S chunks); unit u's part in chunk c is its
+    segment c - (chunk of its first tile).  Returns {u: [(tile_lo, tile_hi)
+    per segment]}."""
+    V = sum(t + 1 for t in unit_tiles if t > 0)
+    tmax = max(unit_tiles)
     need = max(-(-tmax // (S - 1)), 1)
-    n = min(grid, max(T // need, 1)) if T else 1
-    bounds = [c * T // n for c in range(n + 1)]
-    parts, start = {}, 0
+    n = min(grid, max(V // need, 1)) if V else 1
+    bounds = [c * V // n for c in range(n + 1)]
+    parts, pos = {}, 0
     for u, t in enumerate(unit_tiles):
+        start = pos + 1 if t else pos
         parts[u] = [(max(bounds[c], start) - start, min(bounds[c + 1], start + t) - start)
                     for c in range(n) if t and bounds[c] < start + t and bounds[c + 1] > start]
-        start += t
+        pos = start + t
     return parts

@@ -2,7 +2,8 @@
 the C header), as restated for the parity tests and for the benchmark's byte
 accounting: both restatements agree, and the rule has the properties the
 kernel relies on -- every unit's tiles covered once, in order, by at most S
-parts, and chunks that differ by at most one tile."""
+parts, and chunks whose positions (tiles plus one overhead position per unit
+with tiles) differ by at most one."""
 import numpy as np
 import pytest
 
@@ -35,25 +36,41 @@ def test_rule_covers_every_tile_once_within_s_parts(seed):
 
 
 @pytest.mark.parametrize("seed", [3, 4])
-def test_chunks_differ_by_at_most_one_tile(seed):
+def test_chunks_differ_by_at_most_one_position(seed):
     for tiles, S, grid in _cases(300, seed):
-        T = sum(tiles)
-        if T == 0:
+        V = sum(t + 1 for t in tiles if t > 0)
+        if V == 0:
             continue
         need = max(-(-max(tiles) // (S - 1)), 1)
-        n = min(grid, max(T // need, 1))
-        sizes = [(c + 1) * T // n - c * T // n for c in range(n)]
+        n = min(grid, max(V // need, 1))
+        sizes = [(c + 1) * V // n - c * V // n for c in range(n)]
         assert max(sizes) - min(sizes) <= 1 and min(sizes) >= need
-        # the parts of all units, chunk by chunk, add up to the chunk sizes
+        # tiles of every unit's parts plus the overhead positions, chunk by
+        # chunk, add up to the chunk sizes
         per_chunk = [0] * n
-        start = 0
-        bounds = [c * T // n for c in range(n + 1)]
+        bounds = [c * V // n for c in range(n + 1)]
+        chunk = lambda x: next(c for c in range(n) if bounds[c] <= x < bounds[c + 1])
+        parts = balanced_parts(tiles, S, grid)
+        pos = 0
         for u, t in enumerate(tiles):
-            for a, b in balanced_parts(tiles, S, grid)[u]:
-                c = next(c for c in range(n) if bounds[c] <= start + a < bounds[c + 1])
-                per_chunk[c] += b - a
-            start += t
+            if t == 0:
+                continue
+            per_chunk[chunk(pos)] += 1  # the overhead position
+            start = pos + 1
+            for a, b in parts[u]:
+                per_chunk[chunk(start + a)] += b - a
+            pos = start + t
         assert per_chunk == sizes
+
+
+def test_a_chunk_crossing_a_unit_start_holds_one_tile_less():
+    # 4 units of 10 tiles on 4 chunks: 44 positions, 11 each; chunk 0 takes
+    # unit 0 whole (overhead + 10 tiles), every chunk one unit
+    assert balanced_parts([10, 10, 10, 10], 4, 4) == {u: [(0, 10)] for u in range(4)}
+    # 2 units of 20 tiles on 3 chunks: 42 positions, 14 each; unit 0 (positions
+    # 1..20) is cut 13 + 7, unit 1 (22..41) 6 + 14: the middle chunk holds
+    # unit 1's overhead position and 13 tiles (7 + 6)
+    assert balanced_parts([20, 20], 4, 3) == {0: [(0, 13), (13, 20)], 1: [(0, 6), (6, 20)]}
 
 
 def test_benchmark_accounting_uses_the_same_rule():
