@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-merge", action="store_true", help="skip the bandwidth-sized merge leg")
     ap.add_argument("--no-fused", action="store_true", help="skip the in-kernel merge comparison")
+    ap.add_argument("--merge-only", action="store_true",
+                    help="time only the bandwidth-sized segment merge and print its figures (for profiling)")
     return ap.parse_args()
 
 
@@ -752,6 +754,11 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     timer = Timer(stream, dev)
     peaks, peak_kind = measured_peaks()
+    if args.merge_only:
+        if rank == 0:
+            print(json.dumps({"merge_only": bandwidth_sized_merge(dev, stream, timer, max(20, min(args.steps, 500)),
+                                                                  peaks)}))
+        return
     wl = make_workload(args.workload, seed=rank, device=dev)
     sb = StepBench(wl, dev, stream, timer)
 
