@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-merge", action="store_true", help="skip the bandwidth-sized merge leg")
     ap.add_argument("--no-fused", action="store_true", help="skip the in-kernel merge comparison")
+    ap.add_argument("--sweep", type=int, default=100, metavar="N",
+                    help="time the first N points of the seeded 100-point sweep (full size, split-K "
+                         "S=16) and add per-point roofline fractions under 'sweep' (0: skip)")
     ap.add_argument("--merge-only", action="store_true",
                     help="time only the bandwidth-sized segment merge and print its figures (for profiling)")
     return ap.parse_args()
@@ -634,6 +637,49 @@ class StepBench:
         return res
 
 
+def sweep_leg(n_points, dev, stream, timer, peaks, peak_kind, reps=10):
+    """The seeded sweep (heads {16,64,128} x batch 1-256 x context 4k-132k x
+    qlen {1,2,4,8} x bf16/fp8 x block {16,64,256}) at full size, each point's
+    step with 16 split-K slots: per point the decode kernel's time and its
+    roofline fraction (HBM-bound or tensor-bound by its intensity against the
+    measured ridge), and a summary per bound."""
+    from mla_decode_speculative_gb300 import workloads
+    points = workloads.sweep_points(100, seed=0)[:n_points]
+    rows = []
+    for p in points:
+        wl = workloads.sweep_workload(p, device=dev, num_segments=16)
+        sb = StepBench(wl, dev, stream, timer)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                timer.flush.zero_()
+                sb.graph.replay()
+        step_ms = float(np.mean(timer(sb.graph, reps)))
+        s = sb.summary(step_ms, sb.parts(reps), peaks, peak_kind)
+        r = s["roofline"]
+        rb = -(-int(max(wl.qlens)) * wl.num_heads // 64)  # 64-row blocks per request
+        rows.append([p.name(), round(kv_bytes(wl) / 1e6, 1), rb, round(step_ms * 1e3, 1),
+                     round(r["avg_launch_ms"] * 1e3, 1), r["bound"], round(r["frac"], 3)])
+        del sb, wl
+        torch.cuda.empty_cache()
+    summ = {}
+    groups = {}
+    for name, _, rb, _, _, bound, frac in rows:
+        dt = "fp8" if "_fp8_" in name else "bf16"
+        groups.setdefault(f"{bound}_rb{'1' if rb == 1 else '2+'}_{dt}", []).append(frac)
+    for key in sorted(groups):
+        fr = sorted(groups[key])
+        summ[key] = {"points": len(fr), "median_frac": fr[len(fr) // 2], "min_frac": fr[0], "max_frac": fr[-1]}
+    big = sorted((x for x in rows if x[5] == "hbm" and x[2] == 1 and "_bf16_" in x[0]), key=lambda x: -x[1])[:10]
+    if big:
+        summ["hbm_rb1_bf16_largest10_median_frac"] = sorted(x[6] for x in big)[len(big) // 2]
+    return {"summary": summ,
+            "columns": ["point", "kv_mb", "row_blocks", "step_us", "decode_us", "bound", "frac"],
+            "points": rows,
+            "note": "decode kernel alone (CUDA events, L2 flushed before each launch); frac of measured "
+                    "HBM (algorithmic bytes) or of measured bf16 (algorithmic FLOPs) by the point's "
+                    "intensity against the measured ridge"}
+
+
 def bandwidth_sized_merge(dev, stream, timer, n, peaks):
     """The segment merge on an instance large enough to be bandwidth-bound: the
     pages' equal split (16 segments per request, [vLLM #51705, 实现拆解 4]) of a
@@ -832,6 +878,7 @@ def main():
                 raise RuntimeError(f"device error {mla.DEVICE_ERRORS.get(code, code)} in fused {name}")
             del fsb
             torch.cuda.empty_cache()
+    sweep = sweep_leg(args.sweep, dev, stream, timer, peaks, peak_kind) if args.sweep > 0 else None
     merge = dict(head.get("merges", {}))
     if not args.no_merge:
         merge["bandwidth_sized"] = bandwidth_sized_merge(dev, stream, timer, n_parts, peaks)
@@ -860,6 +907,8 @@ def main():
             "workloads": {k: v for k, v in extra.items()},
             "fused_merge": fused_cmp or None,
             "clocks_whole_run": clocks_all}
+    if sweep is not None:
+        line["sweep"] = sweep
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_cpu_baseline(wl, args.cpu_seconds)
     if rank == 0:

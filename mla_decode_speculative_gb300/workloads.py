@@ -261,11 +261,13 @@ def sweep_points(n: int = 100, seed: int = 0) -> List[SweepPoint]:
     return pts
 
 
-def sweep_workload(p: SweepPoint, device=None, max_tokens: Optional[int] = None) -> Workload:
+def sweep_workload(p: SweepPoint, device=None, max_tokens: Optional[int] = None,
+                   num_segments: int = 1) -> Workload:
     """Per-request seq_len U{qlen .. context}; optional cap on total tokens."""
     g = _gen(p.seed + 4000)
     L = torch.randint(p.qlen, p.context + 1, (p.batch,), generator=g).numpy()
     if max_tokens is not None and L.sum() > max_tokens:
         L = np.maximum(p.qlen, (L * (max_tokens / float(L.sum())))).astype(np.int32)
-    return make_workload(p.name(), L, [p.qlen] * p.batch, p.heads, p.block_size,
-                         p.kv_dtype, 1, 1, p.seed, device=device)
+    name = p.name() + (f"_s{num_segments}" if num_segments > 1 else "")
+    return make_workload(name, L, [p.qlen] * p.batch, p.heads, p.block_size,
+                         p.kv_dtype, 1, num_segments, p.seed, device=device)
