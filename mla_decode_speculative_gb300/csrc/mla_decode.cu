@@ -18,11 +18,13 @@
 //    verify row); several row views of the same queries (the shard views of a
 //    DCP step) can share one launch.
 //  * Persistent CTAs, one per SM.  Balanced split (default): every CTA
-//    tabulates the tiles of all (view, request, row block) units, and the
-//    producer warp claims equal chunks of the units' concatenated tiles from
-//    an atomic counter; a chunk's part of each unit it meets is one segment
-//    of that unit.  With the pages' equal split the producer claims (unit,
-//    segment) items, longest requests first.  Entries, with their rows'
+//    tabulates the tiles of all (view, request, row block) units, counts one
+//    overhead position per unit with tiles (a part's Q load and epilogue),
+//    and CTA c takes chunk c of the concatenated positions (the in-kernel
+//    merge variant claims chunks from an atomic counter); a chunk's part of
+//    each unit whose tiles it meets is one segment of that unit.  With the
+//    pages' equal split the producer claims (unit, segment) items from an
+//    atomic counter, longest requests first.  Entries, with their rows'
 //    visible lengths, go to the other roles through a 4-deep shared-memory
 //    work ring.  Every barrier phase follows one running tile counter.
 //  * Swapped operand order, so the output accumulator fits TMEM densely:
@@ -46,6 +48,9 @@
 //    exceeds it by more than 2^8, so O is rarely rescaled in TMEM.
 //  * Every wait is bounded; a timeout records MLA_DEV_WAIT_TIMEOUT, lets all
 //    roles drain without skipping a barrier, frees TMEM and returns.
+//  * Launched with programmatic stream serialization: barriers and TMEM are
+//    set up while the previous kernel in the stream finishes, and nothing
+//    touches global memory before griddepcontrol.wait.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -165,7 +170,7 @@ struct Params {
   int num_rows;
   int max_len;
   int tile3d;              // KV tensor map is the 3-D whole-tile view (page size >= 64)
-  int balanced;            // split-K by equal chunks of the batch's tiles (else S equal segments per request)
+  int balanced;            // split-K by equal chunks of the units' positions (else S equal segments per request)
   int fused;               // balanced split merged in this kernel into out / lse (no merge launch)
   int num_units;           // num_views * num_reqs * row_blocks
   float score_scale_log2;  // sm_scale * kv_scale * log2(e)
@@ -695,9 +700,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ======================================================== producer warp
-    // Claims work items (atomic counter), publishes them to the other roles
-    // through the work ring, and issues the item's TMA loads: Q once, then
-    // every tile into the next free stage.
+    // Takes its chunk (balanced split) or claims work items (atomic
+    // counter), publishes the entries to the other roles through the work
+    // ring, and issues each entry's TMA loads: Q once, then every tile into
+    // the next free stage.
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
     if (lane == 0) {

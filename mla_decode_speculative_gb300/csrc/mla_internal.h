@@ -79,7 +79,7 @@ struct DecodeLaunch {
   uint16_t *segm_out;  // bf16
   float *segm_max;
   float *segm_sum;
-  int *sched;           // work-claim counter (workspace), zeroed before each launch
+  int *sched;           // work-claim counter (workspace), zeroed before a launch that reads it
   unsigned *unit_state; // per-unit part counters (workspace, after sched), zeroed with it
   size_t state_bytes;   // bytes from sched through the unit counters
   int *err;
