@@ -726,29 +726,23 @@ def bandwidth_sized_merge(dev, stream, timer, n, peaks):
 
 def e2e_leg(sb, dev, stream, world, dist):
     """The same metric end to end through the public API: each step copies its
-    inputs (q, seq_lens, qo_indptr, block tables) from pinned host memory,
-    runs the step's library calls and copies out + LSE back to pinned host
-    memory; the copies and the calls are captured as one CUDA graph, replayed
-    and synchronised once per step.  The KV cache stays resident on the device
-    (it is the server's state, not a step input)."""
+    inputs (q, seq_lens, qo_indptr, block tables, packed in one pinned block)
+    to the device in one copy, runs the step's library calls and copies out +
+    LSE back to pinned host memory in one copy; the copies and the calls are
+    captured as one CUDA graph, replayed and synchronised once per step.  The
+    KV cache stays resident on the device (it is the server's state, not a
+    step input)."""
+    from mla_decode_speculative_gb300 import runner
     wl, st = sb.wl, sb.step
-    h_q = wl.q.pin_memory()
-    h_seq = torch.as_tensor(wl.seq_lens, dtype=torch.int32).pin_memory()
-    h_ind = torch.as_tensor(wl.qo_indptr, dtype=torch.int32).pin_memory()
-    h_bt = torch.as_tensor(wl.block_tables, dtype=torch.int32).pin_memory()
-    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h_lse = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
-    d_q, d_seq, d_ind, d_bt = (torch.empty_like(x, device=dev) for x in (h_q, h_seq, h_ind, h_bt))
+    io = runner.StepIO(st, wl.q.shape, wl.num_reqs, wl.block_tables.shape, device=dev)
+    io.stage(wl.q, wl.seq_lens, wl.qo_indptr, wl.block_tables)
+    d_q, d_seq, d_ind, d_bt = io.device_inputs()
     kv = sb.inputs[1]
 
     def api_step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_seq.copy_(h_seq, non_blocking=True)
-        d_ind.copy_(h_ind, non_blocking=True)
-        d_bt.copy_(h_bt, non_blocking=True)
-        o, l = st(d_q, kv, d_seq, d_ind, d_bt, wl.sm_scale, wl.kv_scale)
-        h_out.copy_(o, non_blocking=True)
-        h_lse.copy_(l, non_blocking=True)
+        io.upload()  # one host-to-device copy of the packed inputs
+        st(d_q, kv, d_seq, d_ind, d_bt, wl.sm_scale, wl.kv_scale)
+        io.download()  # one device-to-host copy of out + lse
 
     def run(fn, n):
         s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -768,14 +762,15 @@ def e2e_leg(sb, dev, stream, world, dist):
     g = capture(stream, api_step)
     ms = max_over_ranks(run(g.replay, n), dist, dev)
     eager_ms = max_over_ranks(run(api_step, n), dist, dev)
-    bi = sum(x.numel() * x.element_size() for x in (h_q, h_seq, h_ind, h_bt))
-    bo = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    bi = io.in_bytes
+    bo = io.host_result.numel()
     kvb = kv_bytes(wl)
     return {"value": world * kvb / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "path": "runner.VerifyStep (C ABI) with pinned host buffers: H2D copies, the step's "
-                    "library calls and the D2H copies captured as one CUDA graph, one "
-                    "synchronisation per step; KV cache resident on the device",
+            "path": "runner.VerifyStep (C ABI) with runner.StepIO: the step's inputs packed in one "
+                    "pinned block (one H2D copy), the step's library calls, out + lse in one D2H "
+                    "copy, captured as one CUDA graph, one synchronisation per step; KV cache "
+                    "resident on the device",
             "eager": {"value": world * kvb / (eager_ms * 1e-3) / 1e9, "ms_per_step": eager_ms,
                       "path": "the same calls issued from Python every step (no graph)"}}
 

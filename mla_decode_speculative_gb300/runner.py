@@ -43,8 +43,13 @@ class VerifyStep:
         self.row_req = torch.empty(num_rows, **i32)
         self.subpage = torch.empty((world_size, num_reqs, self.sp_stride), **i32)
         self.row_len_local = torch.empty((world_size, num_rows), **i32)
-        self.out = torch.empty((num_rows, num_heads, mla.D_V), dtype=torch.bfloat16, device=dev)
-        self.lse = torch.empty((num_rows, num_heads), dtype=torch.float32, device=dev)
+        # out and lse share one allocation (lse 256-byte aligned after out), so
+        # a caller reads a step's result back in one copy (``StepIO``)
+        out_bytes = num_rows * num_heads * mla.D_V * 2
+        self.lse_offset = (out_bytes + 255) & ~255
+        self.result = torch.empty(self.lse_offset + num_rows * num_heads * 4, dtype=torch.uint8, device=dev)
+        self.out = self.result[:out_bytes].view(torch.bfloat16).view(num_rows, num_heads, mla.D_V)
+        self.lse = self.result[self.lse_offset:].view(torch.float32).view(num_rows, num_heads)
         if world_size > 1:
             self.part_out = torch.empty((world_size, num_rows, num_heads, mla.D_V),
                                         dtype=torch.bfloat16, device=dev)
@@ -86,6 +91,61 @@ class VerifyStep:
                           uniform_segments=self.uniform, fused_merge=self.fused)
         mla.merge_states(self.part_out, self.part_lse, out=self.out, lse=self.lse, stream=stream)
         return self.out, self.lse
+
+
+class StepIO:
+    """One step's host <-> device traffic in two copies.  The inputs (q,
+    seq_lens, qo_indptr, block tables) live in one pinned host block and one
+    device block at 256-byte aligned offsets; ``upload`` is a single
+    host-to-device copy, after which ``device_inputs`` are views of the device
+    block of the dtypes and shapes ``VerifyStep`` takes.  ``download`` copies the
+    step's ``result`` block (out + lse) back in one device-to-host copy;
+    ``out`` / ``lse`` are views of the pinned result block."""
+
+    def __init__(self, step: VerifyStep, q_shape, num_reqs: int, block_tables_shape, device="cuda"):
+        dev = torch.device(device)
+        a256 = lambda x: (x + 255) & ~255
+        specs = [("q", torch.bfloat16, tuple(q_shape)), ("seq_lens", torch.int32, (num_reqs,)),
+                 ("qo_indptr", torch.int32, (num_reqs + 1,)),
+                 ("block_tables", torch.int32, tuple(block_tables_shape))]
+        self._layout, off = [], 0
+        for name, dt, shape in specs:
+            n = 1
+            for d in shape:
+                n *= int(d)
+            nbytes = n * torch.tensor([], dtype=dt).element_size()
+            self._layout.append((name, dt, shape, off, nbytes))
+            off = a256(off + nbytes)
+        self.in_bytes = off
+        self.host_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self.dev_in = torch.empty(off, dtype=torch.uint8, device=dev)
+        self.step = step
+        self.host_result = torch.empty(step.result.numel(), dtype=torch.uint8).pin_memory()
+        out_bytes = step.out.numel() * 2
+        self.out = self.host_result[:out_bytes].view(torch.bfloat16).view(step.out.shape)
+        self.lse = self.host_result[step.lse_offset:].view(torch.float32).view(step.lse.shape)
+
+    def _view(self, buf, name):
+        for n, dt, shape, off, nbytes in self._layout:
+            if n == name:
+                return buf[off:off + nbytes].view(dt).view(shape)
+        raise KeyError(name)
+
+    def stage(self, q, seq_lens, qo_indptr, block_tables):
+        """Packs a step's host inputs into the pinned block (host memory only)."""
+        for name, x in (("q", q), ("seq_lens", seq_lens), ("qo_indptr", qo_indptr),
+                        ("block_tables", block_tables)):
+            self._view(self.host_in, name).copy_(torch.as_tensor(x).to(self._view(self.host_in, name).dtype))
+
+    def upload(self):
+        self.dev_in.copy_(self.host_in, non_blocking=True)
+
+    def device_inputs(self):
+        """(q, seq_lens, qo_indptr, block_tables) views of the device block."""
+        return tuple(self._view(self.dev_in, n) for n in ("q", "seq_lens", "qo_indptr", "block_tables"))
+
+    def download(self):
+        self.host_result.copy_(self.step.result, non_blocking=True)
 
 
 def step_for_workload(wl, device="cuda", num_segments: Optional[int] = None,
