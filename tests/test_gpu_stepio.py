@@ -11,17 +11,19 @@ from mla_decode_speculative_gb300 import mla, runner, workloads
 pytestmark = pytest.mark.gpu
 
 
-def _workloads():
-    yield workloads.make_workload("stepio_w1", [700, 1300, 90, 2100], [4, 2, 1, 3], 16, 64,
-                                  num_segments=4, seed=61, device="cuda")
-    yield workloads.make_workload("stepio_w4", [3000, 5100, 800], [4, 4, 2], 16, 64, world_size=4,
-                                  num_segments=3, seed=62, device="cuda",
-                                  max_kv_len=-(-5100 // 4))
+# (name, seq_lens, qlens, world size, segment slots, seed); drawn inside the test
+SPECS = [
+    ("stepio_w1", [700, 1300, 90, 2100], [4, 2, 1, 3], 1, 4, 61),
+    ("stepio_w4", [3000, 5100, 800], [4, 4, 2], 4, 3, 62),
+]
 
 
-@pytest.mark.parametrize("wl", list(_workloads()), ids=lambda w: w.name)
+@pytest.mark.parametrize("spec", SPECS, ids=lambda s: s[0])
 @pytest.mark.parametrize("graph", [False, True])
-def test_staged_io_matches_separate_copies_and_the_oracle(wl, graph):
+def test_staged_io_matches_separate_copies_and_the_oracle(spec, graph):
+    name, L, ql, W, S, seed = spec
+    wl = workloads.make_workload(name, L, ql, 16, 64, world_size=W, num_segments=S, seed=seed, device="cuda",
+                                 max_kv_len=-(-max(L) // W))
     ref_step = runner.step_for_workload(wl, "cuda")
     q, kv, seq, ind, bt = runner.device_inputs(wl, "cuda")
     ref_out, ref_lse = ref_step(q, kv, seq, ind, bt, wl.sm_scale, wl.kv_scale)
