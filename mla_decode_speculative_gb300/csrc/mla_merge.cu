@@ -89,10 +89,14 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-constexpr int kOctRing = 8;   // segment merge: parts in the ring (kOctRing - 1 in flight)
-constexpr int kOctCtas = 3;   // segment merge: CTAs per SM
 constexpr int kOctSlot = 8 * 1024;  // one part's octet: [512 dims][8 rows] bf16
-constexpr int kOctDyn = kOctRing * kOctSlot;
+// Two shapes of the segment merge: a deep ring (8 slots, 3 CTAs per SM) for
+// grids of up to two waves -- few units, each with many parts to stream --
+// and a shallower ring at higher occupancy (6 slots, 4 CTAs per SM, <= 64
+// registers) for larger grids, where resident CTAs count more than parts in
+// flight (the bandwidth-sized merge: 0.82 -> 0.85 of measured HBM).
+constexpr int kOctRingDeep = 8, kOctCtasDeep = 3;
+constexpr int kOctRingWide = 6, kOctCtasWide = 4;
 
 // grid (V * B * RB * 8), 256 threads: one (view, request, row block) unit x
 // one row octet (8 rows).  Warp r takes the statistics of row r of the octet:
@@ -109,6 +113,7 @@ constexpr int kOctDyn = kOctRing * kOctSlot;
 // request's first segments hold its tokens; one that turns out empty just
 // gets weight 0, which selects 0), so that their round trip overlaps the
 // statistics'.  Each output row leaves as 128-byte warp stores.
+template <int kOctRing, int kOctCtas>
 __global__ void __launch_bounds__(256, kOctCtas) merge_segment_octets(const SegParams p) {
   grid_dep_wait();
   grid_dep_launch();
@@ -400,7 +405,8 @@ __global__ void __launch_bounds__(kThreadsPerItem) merge_states(const StateParam
 
 // Per device: the segment merge's shared-memory attribute is set (relaxed
 // atomics: concurrent first calls store the same value).
-std::atomic<bool> g_seg_attr_set[64];
+std::atomic<bool> g_seg_attr_set[2][64];  // [shape][device]
+std::atomic<int> g_seg_sms[64];
 
 }  // namespace
 
@@ -431,17 +437,26 @@ mla_status launch_merge(const MergeLaunch &m, cudaStream_t stream) {
       set_error("device ordinal %d out of range", dev);
       return MLA_ERR_CUDA;
     }
-    if (!g_seg_attr_set[dev].load(std::memory_order_relaxed)) {
-      e0 = cudaFuncSetAttribute(merge_segment_octets, cudaFuncAttributeMaxDynamicSharedMemorySize, kOctDyn);
+    int sms = g_seg_sms[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+      e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e0 != cudaSuccess) return cuda_fail(e0, "cudaDeviceGetAttribute(SM count)");
+      g_seg_sms[dev].store(sms, std::memory_order_relaxed);
+    }
+    // more than two waves at the deep shape's occupancy: take the wide shape
+    const bool wide = ctas * 8 > 2 * static_cast<int64_t>(kOctCtasDeep) * sms;
+    auto kern = wide ? merge_segment_octets<kOctRingWide, kOctCtasWide> : merge_segment_octets<kOctRingDeep, kOctCtasDeep>;
+    const int dyn = (wide ? kOctRingWide : kOctRingDeep) * kOctSlot;
+    if (!g_seg_attr_set[wide][dev].load(std::memory_order_relaxed)) {
+      e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
       if (e0 != cudaSuccess) return cuda_fail(e0, "cudaFuncSetAttribute(merge smem)");
-      g_seg_attr_set[dev].store(true, std::memory_order_relaxed);
+      g_seg_attr_set[wide][dev].store(true, std::memory_order_relaxed);
     }
     if (ctas * 8 > INT32_MAX) {
       set_error("mla_merge_segments: too many row blocks (%lld)", (long long)ctas);
       return MLA_ERR_UNSUPPORTED;
     }
-    const cudaError_t el = launch_pdl(merge_segment_octets, dim3(static_cast<unsigned>(ctas * 8)), dim3(256), kOctDyn,
-                                      stream, p);
+    const cudaError_t el = launch_pdl(kern, dim3(static_cast<unsigned>(ctas * 8)), dim3(256), dyn, stream, p);
     if (el != cudaSuccess) return cuda_fail(el, "merge launch");
   } else {
     StateParams p{};
