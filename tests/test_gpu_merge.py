@@ -11,8 +11,12 @@ from mla_decode_speculative_gb300 import mla
 pytestmark = pytest.mark.gpu
 
 
+# the last two cases have more than two waves of row-octet tasks, so the merge
+# takes its wide shape (6-slot ring), with up to 16 / 12 live parts per row to
+# wrap the ring, and partial octets (15 rows per block)
 @pytest.mark.parametrize("qlens,H,S", [([1, 2], 16, 1), ([4] * 32, 16, 16), ([3, 1, 2, 1], 12, 5),
-                                       ([1, 1], 4, 40), ([8, 3], 16, 3)])
+                                       ([1, 1], 4, 40), ([8, 3], 16, 3), ([4] * 160, 8, 16),
+                                       ([3] * 200, 5, 12)])
 def test_merge_segments_matches_oracle(qlens, H, S):
     qo = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
     T = int(qo[-1])
