@@ -1190,7 +1190,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&misc.work_empty[ws]));
         continue;
       }
-      const int *lens_h = &e.lens[32 * g_col + 16 * half];
+      // this thread's 16 columns' visible lengths, constant over the entry's tiles
+      int lv[16];
+      {
+        const int *lens_h = &e.lens[32 * g_col + 16 * half];
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const int4 l4 = *reinterpret_cast<const int4 *>(&lens_h[4 * j4]);
+          lv[4 * j4 + 0] = l4.x;
+          lv[4 * j4 + 1] = l4.y;
+          lv[4 * j4 + 2] = l4.z;
+          lv[4 * j4 + 3] = l4.w;
+        }
+      }
       float l_part[16];
       float m_col[16];  // reference max of this thread's 16 columns (lane c keeps m_ref of group column c)
 #pragma unroll
@@ -1250,15 +1262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gtok = tok0 + tok;
         const bool tok_in = tok < n_valid;
 #pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4) {
-          const int4 lens = *reinterpret_cast<const int4 *>(&lens_h[4 * j4]);
-          const int lv[4] = {lens.x, lens.y, lens.z, lens.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = 4 * j4 + u;
-            x[j] = (tok_in && gtok < lv[u]) ? __uint_as_float(sv[j]) * p.score_scale_log2 : -INFINITY;
-          }
-        }
+        for (int j = 0; j < 16; ++j)
+          x[j] = (tok_in && gtok < lv[j]) ? __uint_as_float(sv[j]) * p.score_scale_log2 : -INFINITY;
         // The column max is needed only when some score exceeds the column's
         // reference by more than the lazy-rescale threshold (always on the
         // first tile that sees data).  One barrier-reduction votes per group.
