@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dcp8", choices=WORKLOADS)
-    ap.add_argument("--extra", default="verify_mtp4,fp8_mixed,wide_rows",
+    ap.add_argument("--extra", default="verify_mtp4,fp8_mixed,wide_rows,decode_qlen1",
                     help="comma-separated workloads also timed into the line ('none': skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -645,6 +645,8 @@ def sweep_leg(n_points, dev, stream, timer, peaks, peak_kind, reps=10):
     measured ridge), and a summary per bound."""
     from mla_decode_speculative_gb300 import workloads
     points = workloads.sweep_points(100, seed=0)[:n_points]
+    if n_points >= 100:  # the sweep's largest corner: 256 requests x 128 heads x qlen 8, context to 132k
+        points.append(workloads.SweepPoint(128, 256, 135168, 8, "bf16", 64, 950))
     rows = []
     for p in points:
         wl = workloads.sweep_workload(p, device=dev, num_segments=16)
